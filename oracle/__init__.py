@@ -1,0 +1,173 @@
+"""CPU oracle for the top-k routed MoE feed-forward layer (TEST INFRASTRUCTURE).
+
+A plain, slow, obviously correct C++ implementation (``oracle.cpp``) of what the
+layer computes, wrapped for numpy.  Only the tests, the smoke check and the
+benchmark's CPU-baseline leg use it; the library never imports it, and it shares
+no code with the CUDA path.  Every function follows the passage cited in
+``oracle.cpp``.
+
+Parity pins (what fixes this oracle independently of itself) live in
+``tests/test_oracle_pins.py`` and ``tests/golden/``.  The absolute layer values
+have no worked example on the pages: they are pinned only through closed forms,
+special cases and brute force (the pins file lists which).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so next to its source (g++, no CUDA, no contraction)."""
+    with _lock:
+        if (not force and os.path.exists(_LIB_PATH)
+                and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            return _LIB_PATH
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-pthread", _SRC, "-o", tmp])
+        os.replace(tmp, _LIB_PATH)
+        return _LIB_PATH
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        lib.oracle_router_logits.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32]
+        lib.oracle_route.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, i32]
+        lib.oracle_load_stats.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
+        lib.oracle_permute.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
+        lib.oracle_expert_ffn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, vp, i32]
+        lib.oracle_combine.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32]
+        lib.oracle_layer_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp,
+                                         vp, vp, i32]
+        for f in ("oracle_router_logits", "oracle_route", "oracle_load_stats", "oracle_permute",
+                  "oracle_expert_ffn", "oracle_combine", "oracle_layer_fwd"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise ValueError(f"{name}: invalid input (code {rc})")
+
+
+def router_logits(x, wr, bias=None, nthreads=0):
+    """l [T, E] fp32: FP32 FMA chain over ascending h, plus bias (one add)."""
+    x = _c(x, np.uint16)
+    wr = _c(wr, np.float32)
+    bias = None if bias is None else _c(bias, np.float32)
+    T, H = x.shape
+    E = wr.shape[1]
+    out = np.empty((T, E), dtype=np.float32)
+    _check(_L().oracle_router_logits(_p(x), _p(wr), _p(bias), T, H, E, _p(out), nthreads),
+           "router_logits")
+    return out
+
+
+def route(x, wr, bias, k, nthreads=0):
+    """(idx [T, k] int32, w [T, k] fp32)."""
+    x = _c(x, np.uint16)
+    wr = _c(wr, np.float32)
+    bias = None if bias is None else _c(bias, np.float32)
+    T, H = x.shape
+    E = wr.shape[1]
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    _check(_L().oracle_route(_p(x), _p(wr), _p(bias), T, H, E, k, _p(idx), _p(w), nthreads),
+           "route")
+    return idx, w
+
+
+def load_stats(idx, E):
+    """(counts [E], offsets [E+1], imbalance max/mean-1, cv)."""
+    idx = _c(idx, np.int32)
+    T, k = idx.shape
+    counts = np.empty(E, dtype=np.int32)
+    offsets = np.empty(E + 1, dtype=np.int32)
+    imb = ctypes.c_double()
+    cv = ctypes.c_double()
+    _check(_L().oracle_load_stats(_p(idx), T, k, E, _p(counts), _p(offsets),
+                                  ctypes.addressof(imb), ctypes.addressof(cv)), "load_stats")
+    return counts, offsets, imb.value, cv.value
+
+
+def permute(x, idx, offsets, E, with_x_perm=True):
+    """(x_perm [T*k, H] bf16 bits or None, row_of_slot [T*k], slot_of_row [T*k])."""
+    x = _c(x, np.uint16)
+    idx = _c(idx, np.int32)
+    offsets = _c(offsets, np.int32)
+    T, H = x.shape
+    k = idx.shape[1]
+    R = T * k
+    x_perm = np.empty((R, H), dtype=np.uint16) if with_x_perm else None
+    ros = np.empty(R, dtype=np.int32)
+    sor = np.empty(R, dtype=np.int32)
+    _check(_L().oracle_permute(_p(x), _p(idx), _p(offsets), T, H, E, k, _p(x_perm), _p(ros),
+                               _p(sor)), "permute")
+    return x_perm, ros, sor
+
+
+def expert_ffn(x_perm, offsets, wg, wu, wd, want_h=False, nthreads=0):
+    """y [R, H] fp32 (and h [R, I] bf16 bits if want_h)."""
+    x_perm = _c(x_perm, np.uint16)
+    offsets = _c(offsets, np.int32)
+    wg, wu, wd = _c(wg, np.uint16), _c(wu, np.uint16), _c(wd, np.uint16)
+    E, H, I = wg.shape
+    R = int(offsets[E])
+    y = np.empty((R, H), dtype=np.float32)
+    h = np.empty((R, I), dtype=np.uint16) if want_h else None
+    _check(_L().oracle_expert_ffn(_p(x_perm), _p(offsets), _p(wg), _p(wu), _p(wd), E, H, I, _p(h),
+                                  _p(y), nthreads), "expert_ffn")
+    return (y, h) if want_h else y
+
+
+def combine(y, w, row_of_slot, nthreads=0):
+    """out [T, H] bf16 bits."""
+    y = _c(y, np.float32)
+    w = _c(w, np.float32)
+    ros = _c(row_of_slot, np.int32).reshape(-1)
+    T, k = w.shape
+    H = y.shape[1]
+    out = np.empty((T, H), dtype=np.uint16)
+    _check(_L().oracle_combine(_p(y), _p(w), _p(ros), T, H, k, _p(out), nthreads), "combine")
+    return out
+
+
+def layer_fwd(x, wr, bias, wg, wu, wd, k, nthreads=0):
+    """(out [T, H] bf16 bits, idx [T, k], w [T, k], counts [E])."""
+    x = _c(x, np.uint16)
+    wr = _c(wr, np.float32)
+    bias = None if bias is None else _c(bias, np.float32)
+    wg, wu, wd = _c(wg, np.uint16), _c(wu, np.uint16), _c(wd, np.uint16)
+    T, H = x.shape
+    E, _, I = wg.shape
+    out = np.empty((T, H), dtype=np.uint16)
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    counts = np.empty(E, dtype=np.int32)
+    _check(_L().oracle_layer_fwd(_p(x), _p(wr), _p(bias), _p(wg), _p(wu), _p(wd), T, H, E, k, I,
+                                 _p(out), _p(idx), _p(w), _p(counts), nthreads), "layer_fwd")
+    return out, idx, w, counts

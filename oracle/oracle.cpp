@@ -1,0 +1,305 @@
+// CPU ORACLE for the top-k routed MoE feed-forward layer forward pass.
+//
+// TEST INFRASTRUCTURE ONLY.  This file is the slow, plain definition that the
+// CUDA path is checked against.  Only the tests, the smoke check and the
+// benchmark's CPU-baseline leg may load it; the library never does.  It shares
+// no code, header, table or helper with the CUDA path.
+//
+// Sources (page title, section):
+//  * "0 train-infer mismatch for open-weight MoE RL", section "Mixture-of-experts
+//    layers / The router": fixed-K projection of each token to one score per
+//    expert, FP32 softmax, top-k selection, the k selected probabilities added
+//    left to right, each divided by that sum, experts returned sorted by
+//    probability.  Same page, "Selecting sparse-attention positions": the lower
+//    position wins a tie (used here for equal logits).
+//  * same page, "SwiGLU: rounding after the multiply": inputs to FP32, SiLU and
+//    the product in FP32, a single cast to BF16.
+//  * same page, "The experts: keeping the route weight inside the accumulator"
+//    and "Sharding the experts": every routing slot is accumulated in FP32 in
+//    slot order and rounded once to BF16.
+//  * "RoutePack: Expert Placement and Attention-Aware Data Packing for MoE RL",
+//    section 2.2 "Routing replay" (Eq. 1: per-expert assignment counts) and
+//    section 2.3 (grouped-GEMM execution of a rank's local experts).
+//  * "FlexFloor", Figure 1: token -> dispatch -> experts -> combine.
+//  * "HARTS", section 3.4 "MoE semantics without expert expansion":
+//    deterministic, no-token-drop top-k routing; Eq. 23 imbalance max/mean - 1.
+//  * RoutePack, section 6 Eq. 22: coefficient of variation of loads.
+//
+// Readings where the pages leave a step open (each stated again where used):
+//  R1 router dot product: FP32 fused multiply-add chain over ascending h from 0,
+//     then one FP32 add of the optional per-expert bias;
+//  R2 selection key: the FP32 logit (softmax is monotone), ties to the lower
+//     expert index; slot order = selection order;
+//  R3 softmax: subtract the max logit, exp in FP32, sum over ascending e;
+//  R4 routing weights stay FP32;
+//  R5 permutation: stable, rows of one expert in ascending token order;
+//  R6 expert GEMMs: FP32 accumulation over ascending K; only h = SwiGLU output is
+//     rounded to BF16; y stays FP32;
+//  R7 combine: FMA chain over slots j = 0..k-1 from 0, one BF16 round.
+//
+// Build: g++ -O2 -std=c++17 -ffp-contract=off (no contraction: every a*b+c below
+// rounds twice unless written as std::fma).
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <thread>
+#include <vector>
+
+namespace {
+
+// bf16 -> f32 is exact: the bf16 bits are the top half of the f32 bits.
+inline float bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+// f32 -> bf16, round to nearest, ties to even (NaN stays NaN).
+inline uint16_t f32_to_bf16(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7FFFu + lsb;
+  return (uint16_t)(u >> 16);
+}
+
+// Run body(i) for i in [0, n) on up to nthreads threads (contiguous chunks).
+void parallel_for(int64_t n, int nthreads, const std::function<void(int64_t)>& body) {
+  if (n <= 0) return;
+  if (nthreads <= 0) nthreads = (int)std::thread::hardware_concurrency();
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > n) nthreads = (int)n;
+  if (nthreads == 1) {
+    for (int64_t i = 0; i < n; ++i) body(i);
+    return;
+  }
+  std::vector<std::thread> pool;
+  for (int w = 0; w < nthreads; ++w) {
+    int64_t b = n * w / nthreads, e = n * (w + 1) / nthreads;
+    pool.emplace_back([b, e, &body] {
+      for (int64_t i = b; i < e; ++i) body(i);
+    });
+  }
+  for (auto& t : pool) t.join();
+}
+
+// Router logits of one token (reading R1).
+void token_logits(const uint16_t* x_row, const float* wr, const float* bias, int H, int E,
+                  float* l) {
+  for (int e = 0; e < E; ++e) l[e] = 0.0f;
+  for (int h = 0; h < H; ++h) {
+    float xf = bf16_to_f32(x_row[h]);
+    const float* wrow = wr + (int64_t)h * E;
+    for (int e = 0; e < E; ++e) l[e] = std::fma(xf, wrow[e], l[e]);
+  }
+  if (bias)
+    for (int e = 0; e < E; ++e) l[e] = l[e] + bias[e];
+}
+
+// Route one token: FP32 softmax, top-k by (logit desc, index asc), renormalise.
+void route_token(const float* l, int E, int k, int32_t* idx, float* w) {
+  // softmax (reading R3)
+  float m = l[0];
+  for (int e = 1; e < E; ++e) m = std::max(m, l[e]);
+  std::vector<float> z(E);
+  float Z = 0.0f;
+  for (int e = 0; e < E; ++e) {
+    z[e] = std::exp(l[e] - m);
+    Z = Z + z[e];
+  }
+  // selection (reading R2): order experts by the key (logit descending, index ascending)
+  std::vector<int> order(E);
+  for (int e = 0; e < E; ++e) order[e] = e;
+  std::sort(order.begin(), order.end(), [&](int a, int b) {
+    if (l[a] != l[b]) return l[a] > l[b];
+    return a < b;
+  });
+  // renormalisation: add the k selected probabilities left to right, divide each by the sum
+  std::vector<float> p(k);
+  float S = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    p[j] = z[order[j]] / Z;
+    S = S + p[j];
+  }
+  for (int j = 0; j < k; ++j) {
+    idx[j] = order[j];
+    w[j] = p[j] / S;
+  }
+}
+
+inline float silu(float g) { return g / (1.0f + std::exp(-g)); }
+
+}  // namespace
+
+extern "C" {
+
+// Router logits l[t, e] (reading R1), for inspection by tests.
+int oracle_router_logits(const uint16_t* x, const float* wr, const float* bias, int T, int H, int E,
+                         float* logits, int nthreads) {
+  if (T < 0 || H <= 0 || E <= 0) return 1;
+  parallel_for(T, nthreads, [&](int64_t t) {
+    token_logits(x + t * H, wr, bias, H, E, logits + t * E);
+  });
+  return 0;
+}
+
+// Step 1-2: router projection, softmax, top-k, renormalisation.
+// x [T, H] bf16 bits; wr [H, E] f32; bias [E] f32 or null -> idx [T, k] int32, w [T, k] f32.
+int oracle_route(const uint16_t* x, const float* wr, const float* bias, int T, int H, int E, int k,
+                 int32_t* idx, float* w, int nthreads) {
+  if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > E) return 1;
+  parallel_for(T, nthreads, [&](int64_t t) {
+    std::vector<float> l(E);
+    token_logits(x + t * H, wr, bias, H, E, l.data());
+    route_token(l.data(), E, k, idx + t * k, w + t * k);
+  });
+  return 0;
+}
+
+// Step 3-4: per-expert assignment counts (RoutePack Eq. 1 summed over tokens),
+// exclusive prefix offsets [E+1], imbalance max/mean - 1 (HARTS Eq. 23 over
+// experts) and coefficient of variation (RoutePack Eq. 22 form over experts).
+int oracle_load_stats(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                      double* imbalance, double* cv) {
+  if (T < 0 || k < 1 || E <= 0) return 1;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int64_t s = 0; s < (int64_t)T * k; ++s) {
+    int e = idx[s];
+    if (e < 0 || e >= E) return 2;
+    counts[e] += 1;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  double mean = (double)T * k / E;
+  double mx = 0.0, var = 0.0;
+  for (int e = 0; e < E; ++e) {
+    mx = std::max(mx, (double)counts[e]);
+    var += ((double)counts[e] - mean) * ((double)counts[e] - mean);
+  }
+  var /= E;
+  if (imbalance) *imbalance = mean > 0 ? mx / mean - 1.0 : 0.0;
+  if (cv) *cv = mean > 0 ? std::sqrt(var) / mean : 0.0;
+  return 0;
+}
+
+// Step 5: stable permutation into expert-contiguous rows (reading R5).
+// Walk slots in token order, then slot order; each takes the next free row of its
+// expert.  slot s = t*k + j.  x_perm[r] is a byte copy of x[slot_of_row[r] / k].
+int oracle_permute(const uint16_t* x, const int32_t* idx, const int32_t* offsets, int T, int H,
+                   int E, int k, uint16_t* x_perm, int32_t* row_of_slot, int32_t* slot_of_row) {
+  if (T < 0 || H <= 0 || E <= 0 || k < 1) return 1;
+  std::vector<int32_t> next(offsets, offsets + E);
+  for (int64_t t = 0; t < T; ++t) {
+    for (int j = 0; j < k; ++j) {
+      int64_t s = t * k + j;
+      int e = idx[s];
+      if (e < 0 || e >= E) return 2;
+      int32_t r = next[e]++;
+      if (r >= offsets[e + 1]) return 3;
+      row_of_slot[s] = r;
+      slot_of_row[r] = (int32_t)s;
+      if (x_perm) std::memcpy(x_perm + (int64_t)r * H, x + t * H, sizeof(uint16_t) * H);
+    }
+  }
+  return 0;
+}
+
+// Steps 6-7: per expert e, rows [offsets[e], offsets[e+1]) of x_perm [R, H]:
+//   g = x W_gate[e], u = x W_up[e]   (FP32 accumulation, ascending h)
+//   h = bf16(silu(g) * u)            (the only rounding, reading R6)
+//   y = h W_down[e]                  (FP32 accumulation, ascending i; FP32 output)
+// W_gate, W_up [E, H, I] and W_down [E, I, H], bf16 bits, row-major.
+// h_out [R, I] (bf16 bits) is optional.
+int oracle_expert_ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* wg,
+                      const uint16_t* wu, const uint16_t* wd, int E, int H, int I, uint16_t* h_out,
+                      float* y, int nthreads) {
+  if (E <= 0 || H <= 0 || I <= 0) return 1;
+  int64_t R = offsets[E];
+  // Each row is independent; expert of row r found by scanning offsets.
+  std::vector<int32_t> expert_of_row(R);
+  for (int e = 0; e < E; ++e)
+    for (int64_t r = offsets[e]; r < offsets[e + 1]; ++r) expert_of_row[r] = e;
+  parallel_for(R, nthreads, [&](int64_t r) {
+    int e = expert_of_row[r];
+    const uint16_t* xr = x_perm + r * H;
+    const uint16_t* Wg = wg + (int64_t)e * H * I;
+    const uint16_t* Wu = wu + (int64_t)e * H * I;
+    const uint16_t* Wd = wd + (int64_t)e * I * H;
+    std::vector<float> g(I, 0.0f), u(I, 0.0f), hf(I);
+    for (int h = 0; h < H; ++h) {
+      float xv = bf16_to_f32(xr[h]);
+      const uint16_t* grow = Wg + (int64_t)h * I;
+      const uint16_t* urow = Wu + (int64_t)h * I;
+      for (int i = 0; i < I; ++i) {
+        g[i] = g[i] + xv * bf16_to_f32(grow[i]);
+        u[i] = u[i] + xv * bf16_to_f32(urow[i]);
+      }
+    }
+    for (int i = 0; i < I; ++i) {
+      uint16_t hb = f32_to_bf16(silu(g[i]) * u[i]);
+      if (h_out) h_out[r * I + i] = hb;
+      hf[i] = bf16_to_f32(hb);
+    }
+    float* yr = y + r * H;
+    for (int c = 0; c < H; ++c) yr[c] = 0.0f;
+    for (int i = 0; i < I; ++i) {
+      float hv = hf[i];
+      const uint16_t* drow = Wd + (int64_t)i * H;
+      for (int c = 0; c < H; ++c) yr[c] = yr[c] + hv * bf16_to_f32(drow[c]);
+    }
+  });
+  return 0;
+}
+
+// Step 8: out[t, c] = bf16(acc), acc = 0; for j = 0..k-1: acc = fma(w[t,j], y[row_of_slot[t*k+j], c], acc)
+// (reading R7).
+int oracle_combine(const float* y, const float* w, const int32_t* row_of_slot, int T, int H, int k,
+                   uint16_t* out, int nthreads) {
+  if (T < 0 || H <= 0 || k < 1) return 1;
+  parallel_for(T, nthreads, [&](int64_t t) {
+    for (int c = 0; c < H; ++c) {
+      float acc = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        int64_t r = row_of_slot[t * k + j];
+        acc = std::fma(w[t * k + j], y[r * H + c], acc);
+      }
+      out[t * H + c] = f32_to_bf16(acc);
+    }
+  });
+  return 0;
+}
+
+// The whole layer: steps 1-8 in order.  Outputs idx/w/counts are optional.
+int oracle_layer_fwd(const uint16_t* x, const float* wr, const float* bias, const uint16_t* wg,
+                     const uint16_t* wu, const uint16_t* wd, int T, int H, int E, int k, int I,
+                     uint16_t* out, int32_t* idx_out, float* w_out, int32_t* counts_out,
+                     int nthreads) {
+  if (T < 0 || H <= 0 || E <= 0 || I <= 0 || k < 1 || k > E) return 1;
+  int64_t R = (int64_t)T * k;
+  std::vector<int32_t> idx(R), counts(E), offsets(E + 1), row_of_slot(R), slot_of_row(R);
+  std::vector<float> w(R);
+  int rc = oracle_route(x, wr, bias, T, H, E, k, idx.data(), w.data(), nthreads);
+  if (rc) return rc;
+  rc = oracle_load_stats(idx.data(), T, k, E, counts.data(), offsets.data(), nullptr, nullptr);
+  if (rc) return rc;
+  std::vector<uint16_t> x_perm((size_t)R * H);
+  rc = oracle_permute(x, idx.data(), offsets.data(), T, H, E, k, x_perm.data(), row_of_slot.data(),
+                      slot_of_row.data());
+  if (rc) return rc;
+  std::vector<float> y((size_t)R * H);
+  rc = oracle_expert_ffn(x_perm.data(), offsets.data(), wg, wu, wd, E, H, I, nullptr, y.data(),
+                         nthreads);
+  if (rc) return rc;
+  rc = oracle_combine(y.data(), w.data(), row_of_slot.data(), T, H, k, out, nthreads);
+  if (rc) return rc;
+  if (idx_out) std::memcpy(idx_out, idx.data(), sizeof(int32_t) * R);
+  if (w_out) std::memcpy(w_out, w.data(), sizeof(float) * R);
+  if (counts_out) std::memcpy(counts_out, counts.data(), sizeof(int32_t) * E);
+  return 0;
+}
+
+}  // extern "C"
