@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Routed MoE layer forward benchmark on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload large] [--impl ours|reference]
+
+One step = one full layer forward (route -> load stats -> permute -> grouped
+gate/up GEMM with SwiGLU -> grouped down GEMM -> combine) over one batch of
+synthetic tokens, through the C ABI (moe_layer_fwd_profiled: the same work as
+moe_layer_fwd plus CUDA events at the step boundaries).  Inputs are resident in
+HBM when the timed region starts; the `e2e` figure repeats the measurement with
+the tokens copied from pinned host memory and the output copied back inside the
+timed region, through moe_layer_fwd.
+
+Metric: routed tokens/s = token->expert assignments (T*k) per second, whole job.
+For N > 1 (torchrun), every rank runs its own replica on its own GPU (tokens are
+independent: weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the max over ranks is taken.
+
+--impl reference times the CPU oracle (the plain C++ definition of the layer) on
+the host cores on a bounded sample of tokens of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "routed tokens/s per MoE layer fwd"
+UNIT = "routed tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="large", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------ distributed ---
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(world, use_cuda):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    dist.init_process_group("nccl" if use_cuda else "gloo")
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, v, device=None):
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks ---
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        smi = shutil.which("nvidia-smi")
+        if smi is None:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.proc = subprocess.Popen([smi, f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits", "-lms", "200"],
+                                     stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained"), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def workload_config(wl, world, l2_note):
+    return {"workload": f"{wl.name}: T={wl.T} H={wl.H} E={wl.E} k={wl.k} I={wl.I}"
+                        + (f", Zipf(s={wl.zipf_s}) router bias" if wl.zipf_s else ", uniform router"),
+            "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
+            "routed_rows_per_step": wl.T * wl.k, "accumulate": "fp32", "router": "fp32",
+            "parallelism": f"replicas x{world} (no data-path collective)", "l2": l2_note,
+            "seed": wl.seed}
+
+
+# ------------------------------------------------------------ CPU oracle ---
+def oracle_sample(wl, x, wr, bias, host_w, S):
+    """Runs the oracle's steps on the first S tokens; returns seconds.  Expert
+    weights are restricted to the experts those tokens use (every row's work is
+    unchanged; only untouched experts are left out)."""
+    import oracle
+    t0 = time.perf_counter()
+    idx, w = oracle.route(x[:S], wr, bias, wl.k)
+    experts = np.unique(idx)
+    remap = np.full(wl.E, -1, np.int64)
+    remap[experts] = np.arange(len(experts))
+    sub_idx = remap[idx].astype(np.int32)
+    counts, offsets, _, _ = oracle.load_stats(sub_idx, len(experts))
+    xp, ros, _ = oracle.permute(x[:S], sub_idx, offsets, len(experts))
+    wg, wu, wd = host_w(experts)
+    y = oracle.expert_ffn(xp, offsets, wg, wu, wd)
+    oracle.combine(y, w, ros)
+    return time.perf_counter() - t0
+
+
+def calibrate_sample(wl, x, wr, bias, host_w, target_s):
+    S = min(wl.T, 8)
+    t = oracle_sample(wl, x, wr, bias, host_w, S)
+    S = int(max(8, min(wl.T, S * target_s / max(t, 1e-3))))
+    return S
+
+
+def host_weight_fn(wl, full=None):
+    if full is not None:
+        wg, wu, wd = full
+        return lambda ex: (wg[ex], wu[ex], wd[ex])
+    return lambda ex: synth.expert_weights(wl, ex)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = synth.WORKLOADS[args.workload]
+    x = synth.tokens(wl)
+    wr, bias = synth.router(wl)
+    host_w = host_weight_fn(wl)
+    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    S = calibrate_sample(wl, x, wr, bias, host_w, per_step)
+    for _ in range(args.warmup):
+        oracle_sample(wl, x, wr, bias, host_w, S)
+    times = [oracle_sample(wl, x, wr, bias, host_w, S) for _ in range(args.steps)]
+    total = sum(times)
+    value = S * wl.k * args.steps / total
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded generator)",
+            "config": workload_config(wl, 1, "host caches (CPU)"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"first {S} of {wl.T} tokens per step ({S * wl.k} routed rows)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# -------------------------------------------------------------- our arm ---
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = dist_init(world, True)
+    import moe_expert_layer_fp32_gb300 as moe
+
+    wl = synth.WORKLOADS[args.workload]
+    T, H, E, k, I = wl.T, wl.H, wl.E, wl.k, wl.I
+    R = T * k
+    d = moe.dims(T, H, E, k, I)
+    x_host = synth.tokens(wl)
+    wr, bias = synth.router(wl)
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+
+    # weights: generated on the host a few experts at a time, uploaded, packed
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(
+        torch.bfloat16)
+    wg_d = torch.empty((E, H, I), dtype=torch.bfloat16, device="cuda")
+    wu_d = torch.empty((E, H, I), dtype=torch.bfloat16, device="cuda")
+    wd_d = torch.empty((E, I, H), dtype=torch.bfloat16, device="cuda")
+    full_host = None
+    if want_cpu:
+        full_host = synth.expert_weights(wl)
+        wg_d.copy_(to_dev(full_host[0]))
+        wu_d.copy_(to_dev(full_host[1]))
+        wd_d.copy_(to_dev(full_host[2]))
+    else:
+        for e0 in range(0, E, 16):
+            ex = list(range(e0, min(E, e0 + 16)))
+            g, u, dn = synth.expert_weights(wl, ex)
+            wg_d[e0:e0 + len(ex)].copy_(to_dev(g))
+            wu_d[e0:e0 + len(ex)].copy_(to_dev(u))
+            wd_d[e0:e0 + len(ex)].copy_(to_dev(dn))
+    packed = moe.prepack(wg_d, wu_d, wd_d, d)
+    torch.cuda.synchronize()
+    del wg_d, wu_d, wd_d
+    torch.cuda.empty_cache()
+
+    x = to_dev(x_host)
+    wr_d = torch.from_numpy(wr).cuda()
+    bias_d = None if bias is None else torch.from_numpy(bias).cuda()
+    ws = moe.new_workspace(d)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+
+    def step():
+        moe.moe_layer_fwd(x, wr_d, bias_d, packed, d, out, idx, w, counts, ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = moe.moe_read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    # ---------------- timed region: inputs resident in HBM -----------------
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    barrier(dist, local)
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record()
+    for i in range(K):
+        moe.moe_layer_fwd_profiled(x, wr_d, bias_d, packed, d, out, idx, w, counts, ws, evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier(dist, local)
+    total_ms = max_over_ranks(dist, start.elapsed_time(end), torch.device("cuda", local))
+    stage_names = ["route", "load_stats", "permute", "gemm_gate_up_swiglu", "gemm_down",
+                   "combine"]
+    stage_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                for j, n in enumerate(stage_names)}
+    status = moe.moe_read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed steps")
+    ms_per_step = total_ms / K
+    value = world * R * K / (total_ms / 1e3)
+
+    # ---------------- roofline of the dominant kernel ----------------------
+    hbm, bf16_burst, bf16_sust, src = peaks()
+    gate_up_flop = 4.0 * R * H * I
+    achieved = gate_up_flop / (stage_ms["gemm_gate_up_swiglu"] / 1e3) / 1e12
+    roofline = {"kernel": "grouped GEMM gate/up + SwiGLU (tcgen05)", "bound": "tensor",
+                "achieved": achieved, "peak": bf16_burst, "unit": "TFLOP/s",
+                "frac": achieved / bf16_burst, "traffic": None,
+                "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)" if src == "measured"
+                else "fallback bf16 burst",
+                "algorithmic": f"4*R*H*I = {gate_up_flop:.4g} FLOP per launch"}
+    down_flop = 2.0 * R * I * H
+    route_flop = 2.0 * T * H * E
+    perm_bytes = T * H * 2 + R * H * 2 + T * k * 4 * 3
+    comb_bytes = R * H * 4 + T * H * 2 + T * k * 8
+    stages = {
+        "route": {"ms": stage_ms["route"], "fp32_tflops": route_flop / stage_ms["route"] / 1e9},
+        "load_stats": {"ms": stage_ms["load_stats"]},
+        "permute": {"ms": stage_ms["permute"],
+                    "hbm_gbs": perm_bytes / stage_ms["permute"] / 1e6},
+        "gemm_gate_up_swiglu": {"ms": stage_ms["gemm_gate_up_swiglu"], "tflops": achieved},
+        "gemm_down": {"ms": stage_ms["gemm_down"],
+                      "tflops": down_flop / stage_ms["gemm_down"] / 1e9},
+        "combine": {"ms": stage_ms["combine"], "hbm_gbs": comb_bytes / stage_ms["combine"] / 1e6},
+    }
+    grouped = (gate_up_flop + down_flop) / ((stage_ms["gemm_gate_up_swiglu"]
+                                             + stage_ms["gemm_down"]) / 1e3) / 1e12
+
+    # ---------------- e2e: host buffers, copies inside the timed region ----
+    x_pin = torch.from_numpy(x_host.view(np.int16)).pin_memory().view(torch.bfloat16)
+    out_pin = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_e = torch.empty_like(x)
+
+    def e2e_step():
+        x_e.copy_(x_pin, non_blocking=True)
+        moe.moe_layer_fwd(x_e, wr_d, bias_d, packed, d, out, None, None, None, ws)
+        out_pin.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(K):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, s2.elapsed_time(e2), torch.device("cuda", local))
+    barrier(dist, local)
+    e2e = {"value": world * R * K / (e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
+           "call": "moe_layer_fwd with pinned host tokens copied in and output copied out"}
+
+    cpu = None
+    if want_cpu:
+        host_w = host_weight_fn(wl, full_host)
+        S = calibrate_sample(wl, x_host, wr, bias, host_w, args.cpu_seconds)
+        t = oracle_sample(wl, x_host, wr, bias, host_w, S)
+        cpu = {"value": S * k / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"first {S} of {T} tokens ({S * k} routed rows), {t:.1f} s"}
+
+    if rank == 0:
+        l2 = f"inputs larger than L2 (tokens {T * H * 2 / 1e6:.0f} MB, packed weights " \
+             f"{E * 3 * H * I * 2 / 1e9:.2f} GB); no flush"
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded generator; random-init weights)",
+                "config": workload_config(wl, world, l2),
+                "tokens_per_s": world * T * K / (total_ms / 1e3),
+                "roofline": roofline, "grouped_gemm_tflops": grouped, "stages": stages,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 8 * K,
+                "clocks": clock_info}
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,195 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) top-k routed Mixture-of-Experts
+ * feed-forward layer forward pass.
+ *
+ * The layer, step by step (sources are the page titles and sections that define
+ * each operation):
+ *
+ *   route        router projection of every token to one score per expert with a
+ *                fixed reduction order, FP32 softmax, top-k, left-to-right
+ *                renormalisation, experts sorted by probability
+ *                ("0 train-infer mismatch for open-weight MoE RL", section
+ *                 "Mixture-of-experts layers / The router")
+ *   load stats   routed-token count per expert and its exclusive prefix sum
+ *                ("RoutePack", section 2.2 "Routing replay", Eq. 1)
+ *   permute      dispatch: stable permutation of token rows into expert-contiguous
+ *                rows ("FlexFloor", Figure 1: token -> dispatch -> experts;
+ *                 "RoutePack", section 2.3: a rank's local experts run as one
+ *                 grouped operation)
+ *   expert FFN   grouped SwiGLU expert GEMMs with one BF16 rounding of the
+ *                intermediate ("0 train-infer mismatch", section "SwiGLU: rounding
+ *                after the multiply")
+ *   combine      per token, the routing slots accumulated in FP32 in slot order,
+ *                rounded once to BF16 ("0 train-infer mismatch", sections
+ *                "Sharding the experts" and "The experts: keeping the route weight
+ *                inside the accumulator")
+ *
+ * Every token is routed to exactly k distinct experts; nothing is dropped
+ * ("HARTS", section "MoE semantics without expert expansion": deterministic,
+ * no-token-drop top-k routing).
+ *
+ * Conventions for every call
+ * --------------------------
+ *  - All tensor pointers are DEVICE pointers, owned by the caller, 16-byte
+ *    aligned, dense and row-major.  bf16 tensors are passed as void*.  The
+ *    library never allocates, frees or keeps device memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are stream-ordered and asynchronous: they return once the work is
+ *    enqueued.
+ *  - Host-side validation happens before anything is launched; a non-OK status
+ *    means nothing was enqueued, except MOE_ERR_CUDA, which reports a failed
+ *    launch or runtime call.
+ *  - Kernels that read indices or offsets from memory check them against the
+ *    dimensions.  A failed check skips the offending access and records
+ *    MOE_ERR_DEVICE_CHECK in the workspace status word; a bounded device-side
+ *    wait that runs out records MOE_ERR_TIMEOUT.  Read (and clear) it with
+ *    moe_read_device_status.  Calls without a workspace argument (moe_route,
+ *    moe_combine) take no status word: moe_combine skips out-of-range rows.
+ *  - Dimensions (moe_dims): T tokens (T >= 0; T = 0 is a no-op), H hidden size,
+ *    E experts, k experts per token, I expert intermediate size.
+ *    Limits: 1 <= E <= 256, 1 <= k <= min(E, 16), H and I multiples of 128,
+ *    H <= 16384, I <= 16384, T*k < 2^31.
+ *  - Batch invariance: no kernel's reduction order, tile shape or launch shape
+ *    depends on T, so a token's output bytes do not depend on which batch it
+ *    is in.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer where one is required, bad dimension */
+  MOE_ERR_UNSUPPORTED = 2,  /* dimension outside the limits above, or no sm_103a device */
+  MOE_ERR_MISALIGNED = 3,   /* pointer not 16-byte aligned (workspace: 256-byte) */
+  MOE_ERR_WORKSPACE = 4,    /* workspace or packed-weight buffer too small */
+  MOE_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 6,      /* device: a bounded wait ran out (read via moe_read_device_status) */
+  MOE_ERR_DEVICE_CHECK = 7  /* device: an index or offset read from memory was out of range */
+} moe_status;
+
+typedef struct {
+  int32_t T, H, E, k, I;
+} moe_dims;
+
+/* Bytes of device workspace that every call taking a workspace needs for these
+ * dimensions (the full layer's need; each step uses a part of the same layout).
+ * The workspace must be 256-byte aligned and its first 256 bytes (the status
+ * word) zero before first use; moe_read_device_status clears them.  The rest is
+ * scratch.  Two calls in flight at once must not share a workspace. */
+size_t moe_workspace_bytes(moe_dims d);
+
+/* Bytes of the packed expert-weight buffer written by moe_prepack_expert_weights:
+ * E * 3 * H * I bf16 values. */
+size_t moe_packed_weight_bytes(moe_dims d);
+
+/* Step: router.  For every token t:
+ *   l[t,e] = ((sum over h = 0..H-1, as an FP32 fused multiply-add chain from 0,
+ *              of float(x[t,h]) * w_router[h,e])) + bias[e]
+ *   p = softmax(l) in FP32; the k experts with the largest l (ties: lower expert
+ *   index first) become slots j = 0..k-1 in that order; S = sum of their p added
+ *   left to right; topk_w[t,j] = p[e_j] / S.
+ *   x        [T, H] bf16
+ *   w_router [H, E] fp32
+ *   bias     [E] fp32 or NULL (a per-expert popularity bias added to the logits)
+ *   topk_idx [T, k] int32 out (expert ids), topk_w [T, k] fp32 out.
+ * The indices are bit-reproducible against a CPU FMA chain; the weights agree
+ * with it to a few FP32 ulp (the exponential differs between math libraries). */
+moe_status moe_route(const void* x, const float* w_router, const float* bias, moe_dims d,
+                     int32_t* topk_idx, float* topk_w, void* stream);
+
+/* Step: per-expert load.  counts[e] = number of (t, j) with topk_idx[t,j] = e;
+ * offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e] (so offsets[E] = T*k).
+ *   topk_idx [T, k] int32 in; counts [E] int32 out; offsets [E+1] int32 out.
+ * Out-of-range ids are skipped and flagged (MOE_ERR_DEVICE_CHECK). */
+moe_status moe_load_stats(const int32_t* topk_idx, moe_dims d, int32_t* counts, int32_t* offsets,
+                          void* workspace, size_t ws_bytes, void* stream);
+
+/* Host-side summary of counts already copied to the host: imbalance
+ * max/mean - 1 ("HARTS", Eq. 23, taken over experts) and the coefficient of
+ * variation std/mean ("RoutePack", Eq. 22 form, one layer, over experts).
+ * Either output pointer may be NULL. */
+moe_status moe_load_summary_host(const int32_t* counts_host, int32_t E, double* imbalance,
+                                 double* cv);
+
+/* Step: dispatch.  Stable permutation into expert-contiguous rows: slot
+ * s = t*k + j with expert e goes to row
+ *   r = offsets[e] + #{ t' < t : token t' chose e },
+ * row_of_slot[s] = r, slot_of_row[r] = s, and x_perm[r, :] = x[t, :] (bytes).
+ *   x [T, H] bf16; topk_idx [T, k]; offsets [E+1] (as moe_load_stats writes them)
+ *   x_perm [T*k, H] bf16 out; row_of_slot [T*k] out; slot_of_row [T*k] out.
+ * Offsets that disagree with topk_idx are flagged (MOE_ERR_DEVICE_CHECK) and
+ * rows that would fall outside [0, T*k) are not written. */
+moe_status moe_permute(const void* x, const int32_t* topk_idx, const int32_t* offsets, moe_dims d,
+                       void* x_perm, int32_t* row_of_slot, int32_t* slot_of_row, void* workspace,
+                       size_t ws_bytes, void* stream);
+
+/* One-time weight preparation (not part of a forward).  Reads the logical
+ * layouts and writes the K-major tiles the grouped GEMMs stream with TMA:
+ *   w_gate [E, H, I] bf16, w_up [E, H, I] bf16, w_down [E, I, H] bf16
+ *   packed: moe_packed_weight_bytes(d) bytes, 16-byte aligned. */
+moe_status moe_prepack_expert_weights(const void* w_gate, const void* w_up, const void* w_down,
+                                      moe_dims d, void* packed, size_t packed_bytes, void* stream);
+
+/* Step: grouped SwiGLU experts.  For each expert e and each row r in
+ * [offsets[e], offsets[e+1]):
+ *   g = x_perm[r] . W_gate[e], u = x_perm[r] . W_up[e]   (BF16 products, FP32 accumulation)
+ *   h[r] = bf16(silu(g) * u)                             (the only rounding)
+ *   y[r] = h[r] . W_down[e]                              (FP32 accumulation, FP32 output)
+ *   x_perm [T*k, H] bf16; offsets [E+1] int32; packed weights from
+ *   moe_prepack_expert_weights; y [T*k, H] fp32 out.  h lives in the workspace.
+ * Offsets that are not a non-decreasing sequence from 0 to T*k are flagged
+ * (MOE_ERR_DEVICE_CHECK) and no row is written. */
+moe_status moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void* packed_weights,
+                          moe_dims d, float* y, void* workspace, size_t ws_bytes, void* stream);
+
+/* Step: combine.  out[t, c] = bf16(acc), acc = 0, then for j = 0..k-1:
+ *   acc = fmaf(topk_w[t,j], y[row_of_slot[t*k+j], c], acc).
+ *   y [T*k, H] fp32; topk_w [T, k] fp32; row_of_slot [T*k] int32; out [T, H] bf16.
+ * Rows outside [0, T*k) contribute nothing. */
+moe_status moe_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, moe_dims d,
+                       void* out, void* stream);
+
+/* The whole layer forward: route -> load stats -> permute -> expert FFN ->
+ * combine, enqueued on one stream with no host synchronisation.
+ *   x [T, H] bf16; w_router [H, E] fp32; bias [E] fp32 or NULL; packed_weights
+ *   from moe_prepack_expert_weights; out [T, H] bf16.
+ *   topk_idx_out [T, k], topk_w_out [T, k] and counts_out [E] are optional
+ *   (NULL: kept in the workspace only). */
+moe_status moe_layer_fwd(const void* x, const float* w_router, const float* bias,
+                         const void* packed_weights, moe_dims d, void* out, int32_t* topk_idx_out,
+                         float* topk_w_out, int32_t* counts_out, void* workspace, size_t ws_bytes,
+                         void* stream);
+
+/* moe_layer_fwd that also records caller-created CUDA events (cudaEvent_t
+ * passed as void*) on `stream` at the step boundaries, for per-step timing:
+ *   events[0] before the router, [1] after it, [2] after the load statistics,
+ *   [3] after the permutation, [4] after the grouped gate/up GEMM (SwiGLU),
+ *   [5] after the grouped down GEMM, [6] after the combine.
+ * n_events must be 7 (or 0 with events NULL, which is moe_layer_fwd).  The work
+ * enqueued is identical to moe_layer_fwd's. */
+moe_status moe_layer_fwd_profiled(const void* x, const float* w_router, const float* bias,
+                                  const void* packed_weights, moe_dims d, void* out,
+                                  int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out,
+                                  void* workspace, size_t ws_bytes, void* stream,
+                                  void* const* events, int32_t n_events);
+
+/* Synchronises `stream`, returns the workspace status word in *status_out
+ * (MOE_OK or the first device-side error recorded since the last read) and
+ * clears it. */
+moe_status moe_read_device_status(void* workspace, int32_t* status_out, void* stream);
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,217 @@
+"""GB300 (sm_103a) top-k routed MoE feed-forward layer forward.
+
+Thin binding over the C ABI in ``include/moe.h`` (``libmoe_gb300.so``): the
+functions below carry the same names and only marshal arguments (torch tensors
+-> device pointers, the current CUDA stream).  Every step runs in the library's
+CUDA kernels; there is no CPU path.  Importing fails loudly when the library has
+not been built (``python moe_expert_layer_fp32_gb300/build.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python moe_expert_layer_fp32_gb300/build.py)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
+          4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT",
+          7: "MOE_ERR_DEVICE_CHECK"}
+
+# Every symbol include/moe.h declares.
+ABI_SYMBOLS = ("moe_workspace_bytes", "moe_packed_weight_bytes", "moe_route", "moe_load_stats",
+               "moe_load_summary_host", "moe_permute", "moe_prepack_expert_weights",
+               "moe_expert_ffn", "moe_combine", "moe_layer_fwd", "moe_layer_fwd_profiled",
+               "moe_read_device_status", "moe_status_string")
+
+
+class moe_dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("I", ctypes.c_int32)]
+
+    def __repr__(self):
+        return f"moe_dims(T={self.T}, H={self.H}, E={self.E}, k={self.k}, I={self.I})"
+
+
+def dims(T, H, E, k, I) -> moe_dims:
+    return moe_dims(T, H, E, k, I)
+
+
+_vp, _sz, _i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+_sig = {
+    "moe_workspace_bytes": (_sz, [moe_dims]),
+    "moe_packed_weight_bytes": (_sz, [moe_dims]),
+    "moe_route": (ctypes.c_int, [_vp, _vp, _vp, moe_dims, _vp, _vp, _vp]),
+    "moe_load_stats": (ctypes.c_int, [_vp, moe_dims, _vp, _vp, _vp, _sz, _vp]),
+    "moe_load_summary_host": (ctypes.c_int, [_vp, _i32, _vp, _vp]),
+    "moe_permute": (ctypes.c_int, [_vp, _vp, _vp, moe_dims, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_prepack_expert_weights": (ctypes.c_int, [_vp, _vp, _vp, moe_dims, _vp, _sz, _vp]),
+    "moe_expert_ffn": (ctypes.c_int, [_vp, _vp, _vp, moe_dims, _vp, _vp, _sz, _vp]),
+    "moe_combine": (ctypes.c_int, [_vp, _vp, _vp, moe_dims, _vp, _vp]),
+    "moe_layer_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, moe_dims, _vp, _vp, _vp, _vp, _vp, _sz,
+                                     _vp]),
+    "moe_layer_fwd_profiled": (ctypes.c_int, [_vp, _vp, _vp, _vp, moe_dims, _vp, _vp, _vp, _vp,
+                                              _vp, _sz, _vp, _vp, _i32]),
+    "moe_read_device_status": (ctypes.c_int, [_vp, _vp, _vp]),
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+for _name, (_res, _args) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+class MoEError(RuntimeError):
+    def __init__(self, name, code):
+        self.code = code
+        super().__init__(f"{name}: {STATUS.get(code, code)} "
+                         f"({_lib.moe_status_string(code).decode()})")
+
+
+def _check(name, code):
+    if code != MOE_OK:
+        raise MoEError(name, code)
+
+
+def _ptr(t):
+    """Device address of a tensor (None -> NULL); an int is taken as an address."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ws(ws):
+    return (_ptr(ws), ws.numel() * ws.element_size()) if isinstance(ws, torch.Tensor) else ws
+
+
+# ------------------------------------------------------------ raw ABI calls ---
+def moe_workspace_bytes(d: moe_dims) -> int:
+    return int(_lib.moe_workspace_bytes(d))
+
+
+def moe_packed_weight_bytes(d: moe_dims) -> int:
+    return int(_lib.moe_packed_weight_bytes(d))
+
+
+def moe_route(x, w_router, bias, d, topk_idx, topk_w, stream=None):
+    _check("moe_route", _lib.moe_route(_ptr(x), _ptr(w_router), _ptr(bias), d, _ptr(topk_idx),
+                                       _ptr(topk_w), _stream(stream)))
+
+
+def moe_load_stats(topk_idx, d, counts, offsets, workspace, stream=None):
+    wp, wb = _ws(workspace)
+    _check("moe_load_stats", _lib.moe_load_stats(_ptr(topk_idx), d, _ptr(counts), _ptr(offsets),
+                                                 wp, wb, _stream(stream)))
+
+
+def moe_load_summary_host(counts_host):
+    """(imbalance max/mean - 1, cv) from host counts (sequence or numpy array)."""
+    import numpy as np
+    c = np.ascontiguousarray(counts_host, dtype=np.int32)
+    imb, cv = ctypes.c_double(), ctypes.c_double()
+    _check("moe_load_summary_host", _lib.moe_load_summary_host(
+        c.ctypes.data, int(c.size), ctypes.addressof(imb), ctypes.addressof(cv)))
+    return imb.value, cv.value
+
+
+def moe_permute(x, topk_idx, offsets, d, x_perm, row_of_slot, slot_of_row, workspace, stream=None):
+    wp, wb = _ws(workspace)
+    _check("moe_permute", _lib.moe_permute(_ptr(x), _ptr(topk_idx), _ptr(offsets), d, _ptr(x_perm),
+                                           _ptr(row_of_slot), _ptr(slot_of_row), wp, wb,
+                                           _stream(stream)))
+
+
+def moe_prepack_expert_weights(w_gate, w_up, w_down, d, packed, stream=None):
+    nbytes = packed.numel() * packed.element_size() if isinstance(packed, torch.Tensor) else 1 << 62
+    _check("moe_prepack_expert_weights", _lib.moe_prepack_expert_weights(
+        _ptr(w_gate), _ptr(w_up), _ptr(w_down), d, _ptr(packed), nbytes, _stream(stream)))
+
+
+def moe_expert_ffn(x_perm, offsets, packed_weights, d, y, workspace, stream=None):
+    wp, wb = _ws(workspace)
+    _check("moe_expert_ffn", _lib.moe_expert_ffn(_ptr(x_perm), _ptr(offsets), _ptr(packed_weights),
+                                                 d, _ptr(y), wp, wb, _stream(stream)))
+
+
+def moe_combine(y, topk_w, row_of_slot, d, out, stream=None):
+    _check("moe_combine", _lib.moe_combine(_ptr(y), _ptr(topk_w), _ptr(row_of_slot), d, _ptr(out),
+                                           _stream(stream)))
+
+
+def moe_layer_fwd(x, w_router, bias, packed_weights, d, out, topk_idx_out, topk_w_out, counts_out,
+                  workspace, stream=None):
+    wp, wb = _ws(workspace)
+    _check("moe_layer_fwd", _lib.moe_layer_fwd(
+        _ptr(x), _ptr(w_router), _ptr(bias), _ptr(packed_weights), d, _ptr(out),
+        _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), wp, wb, _stream(stream)))
+
+
+def moe_layer_fwd_profiled(x, w_router, bias, packed_weights, d, out, topk_idx_out, topk_w_out,
+                           counts_out, workspace, events, stream=None):
+    """``events``: 7 torch.cuda.Event(enable_timing=True) recorded at the step
+    boundaries (before route, after route, load stats, permute, gate/up GEMM,
+    down GEMM, combine)."""
+    wp, wb = _ws(workspace)
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check("moe_layer_fwd_profiled", _lib.moe_layer_fwd_profiled(
+        _ptr(x), _ptr(w_router), _ptr(bias), _ptr(packed_weights), d, _ptr(out),
+        _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), wp, wb, _stream(stream), arr,
+        len(events)))
+
+
+def moe_read_device_status(workspace, stream=None) -> int:
+    v = ctypes.c_int32()
+    wp, _ = _ws(workspace)
+    _check("moe_read_device_status", _lib.moe_read_device_status(wp, ctypes.addressof(v),
+                                                                 _stream(stream)))
+    return v.value
+
+
+# ------------------------------------------------- allocation conveniences ---
+# (torch's allocator supplies the memory; the library itself allocates nothing)
+def new_workspace(d: moe_dims, device="cuda") -> torch.Tensor:
+    """Zeroed workspace of moe_workspace_bytes(d) bytes (256-byte aligned by torch)."""
+    n = moe_workspace_bytes(d)
+    if n == 0:
+        raise MoEError("moe_workspace_bytes", 2)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def prepack(w_gate, w_up, w_down, d, stream=None) -> torch.Tensor:
+    packed = torch.empty(moe_packed_weight_bytes(d) // 2, dtype=torch.bfloat16,
+                         device=w_gate.device)
+    moe_prepack_expert_weights(w_gate, w_up, w_down, d, packed, stream)
+    return packed
+
+
+def layer_forward(x, w_router, bias, packed, d, workspace, stream=None, want_routing=False):
+    """out [T, H] bf16 (and topk_idx, topk_w, counts if want_routing)."""
+    dev = x.device
+    out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
+    idx = w = counts = None
+    if want_routing:
+        idx = torch.empty((d.T, d.k), dtype=torch.int32, device=dev)
+        w = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
+        counts = torch.empty(d.E, dtype=torch.int32, device=dev)
+    moe_layer_fwd(x, w_router, bias, packed, d, out, idx, w, counts, workspace, stream)
+    return (out, idx, w, counts) if want_routing else out

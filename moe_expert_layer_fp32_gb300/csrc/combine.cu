@@ -1,0 +1,71 @@
+// Combine: the weighted sum of a token's k expert outputs, in slot order.
+//
+// "0 train-infer mismatch for open-weight MoE RL", section "Sharding the
+// experts": every routing slot is accumulated in FP32 in slot order and rounded
+// once to BF16; section "The experts: keeping the route weight inside the
+// accumulator": the route weight multiplies the FP32 down-projection value
+// before the single rounding.  Here: acc = 0, acc = fmaf(w[t,j], y[row_j, c], acc)
+// for j = 0..k-1, out = bf16(acc).
+//
+// Memory-bound gather: one CTA per token, 16-byte loads of the k FP32 rows
+// (all issued before the FMA chain), 8-byte stores of four bf16 outputs.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ y,
+                                                      const float* __restrict__ topk_w,
+                                                      const int32_t* __restrict__ row_of_slot,
+                                                      int T, int H, int k,
+                                                      uint16_t* __restrict__ out) {
+  __shared__ int s_row[kMaxK];
+  __shared__ float s_w[kMaxK];
+  const int t = blockIdx.x;
+  const long long R = (long long)T * k;
+  if (threadIdx.x < k) {
+    const int r = row_of_slot[(size_t)t * k + threadIdx.x];
+    s_row[threadIdx.x] = (r >= 0 && r < R) ? r : -1;
+    s_w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  int row[kMaxK];
+  float w[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    row[j] = (j < k) ? s_row[j] : -1;
+    w[j] = (j < k) ? s_w[j] : 0.0f;
+  }
+  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+    float4 v[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (row[j] >= 0) v[j] = __ldg(reinterpret_cast<const float4*>(y + (size_t)row[j] * H + c));
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (row[j] >= 0) {
+        a0 = fmaf(w[j], v[j].x, a0);
+        a1 = fmaf(w[j], v[j].y, a1);
+        a2 = fmaf(w[j], v[j].z, a2);
+        a3 = fmaf(w[j], v[j].w, a3);
+      }
+    }
+    uint2 o;
+    o.x = pack_bf16x2(a0, a1);
+    o.y = pack_bf16x2(a2, a3);
+    *reinterpret_cast<uint2*>(out + (size_t)t * H + c) = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, int T,
+                           int H, int k, void* out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  combine_kernel<<<T, 128, 0, s>>>(y, topk_w, row_of_slot, T, H, k, static_cast<uint16_t*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

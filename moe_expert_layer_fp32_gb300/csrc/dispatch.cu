@@ -1,0 +1,235 @@
+// Load statistics and dispatch: per-expert counts, exclusive offsets, and the
+// stable permutation of token rows into expert-contiguous rows.
+//
+// "RoutePack", section 2.2 "Routing replay" (Eq. 1): the load of expert e is the
+// number of token->expert assignments.  Section 2.3: a rank's local experts run
+// as one grouped operation, which needs each expert's rows contiguous.
+// "FlexFloor", Figure 1: token -> dispatch -> experts -> combine.
+//
+// Determinism without float atomics or sorting.  Tokens are cut into blocks of
+// 256 (8 warps x 32 lanes, one token per lane).  For each warp and expert a
+// 32-bit mask of the lanes whose token chose that expert is built with integer
+// atomicOr (order-free).  A token's stable rank inside its block is then
+//   popc(mask[w][e] & lanes_below) + sum_{w' < w} popc(mask[w'][e]),
+// the block's count of e is sum_w popc(mask[w][e]), and one scan kernel turns
+// per-block counts into per-(block, expert) first rows.  Every quantity is an
+// integer function of topk_idx alone: bit-identical on every run and for every T.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int PB = kPermBlock;  // 256 tokens, 8 warps
+
+// Builds masks[w][e] for the block's tokens; returns nothing but fills smem.
+// sidx holds the block's topk_idx rows.  Invalid ids and repeated experts within
+// one token are flagged and left out.
+__device__ __forceinline__ void build_masks(const int32_t* __restrict__ topk_idx, int T, int k,
+                                            int E, int t0, uint32_t* masks, int32_t* sidx,
+                                            int32_t* status) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ntok = min(PB, T - t0);
+  const int n = ntok * k;
+  const int32_t* src = topk_idx + (size_t)t0 * k;
+  for (int i = tid; i < n; i += blockDim.x) sidx[i] = __ldg(src + i);
+  for (int i = tid; i < 8 * E; i += blockDim.x) masks[i] = 0u;
+  __syncthreads();
+  const int tl = warp * 32 + lane;
+  if (tl < ntok) {
+    for (int j = 0; j < k; ++j) {
+      const int e = sidx[tl * k + j];
+      if (e < 0 || e >= E) {
+        flag_error(status, MOE_ERR_DEVICE_CHECK);
+        continue;
+      }
+      const uint32_t old = atomicOr(&masks[warp * E + e], 1u << lane);
+      if (old & (1u << lane)) flag_error(status, MOE_ERR_DEVICE_CHECK);  // expert repeated
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(PB) block_counts_kernel(const int32_t* __restrict__ topk_idx,
+                                                          int T, int k, int E,
+                                                          int32_t* __restrict__ blk_counts,
+                                                          int32_t* status) {
+  extern __shared__ uint32_t smem_u[];
+  uint32_t* masks = smem_u;                               // [8][E]
+  int32_t* sidx = reinterpret_cast<int32_t*>(smem_u + 8 * E);  // [PB*k]
+  const int b = blockIdx.x;
+  build_masks(topk_idx, T, k, E, b * PB, masks, sidx, status);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) c += __popc(masks[w * E + e]);
+    blk_counts[(size_t)b * E + e] = c;
+  }
+}
+
+// One CTA, one thread per expert: running sums over blocks, then an exclusive
+// scan over experts for the offsets.
+__global__ void __launch_bounds__(kMaxE) scan_kernel(const int32_t* __restrict__ blk_counts, int nb,
+                                                     int E, int R, int32_t* __restrict__ counts,
+                                                     int32_t* __restrict__ offsets,
+                                                     int offsets_given,
+                                                     int32_t* __restrict__ blk_base,
+                                                     int32_t* status) {
+  __shared__ int s_scan[kMaxE];
+  __shared__ int s_bad;
+  const int e = threadIdx.x;
+  if (e == 0) s_bad = 0;
+  int running = 0;
+  if (e < E) {
+    for (int b = 0; b < nb; ++b) {
+      const int c = blk_counts[(size_t)b * E + e];
+      blk_base[(size_t)b * E + e] = running;
+      running += c;
+    }
+  }
+  // inclusive Hillis-Steele scan over the (padded) expert axis
+  s_scan[e] = (e < E) ? running : 0;
+  __syncthreads();
+  for (int off = 1; off < kMaxE; off <<= 1) {
+    const int v = (e >= off) ? s_scan[e - off] : 0;
+    __syncthreads();
+    s_scan[e] += v;
+    __syncthreads();
+  }
+  const int excl = s_scan[e] - ((e < E) ? running : 0);
+  const int total = s_scan[kMaxE - 1];
+  int base = excl;
+  if (offsets_given) {
+    if (e < E) {
+      const int a = offsets[e], bnext = offsets[e + 1];
+      if (a != excl || bnext - a != running) atomicOr(&s_bad, 1);
+    }
+    if (e == 0 && (offsets[0] != 0 || offsets[E] != R)) atomicOr(&s_bad, 1);
+  } else {
+    if (e < E) offsets[e] = excl;
+    if (e == 0) offsets[E] = total;
+  }
+  if (e == 0 && total != R) atomicOr(&s_bad, 1);
+  if (counts != nullptr && e < E) counts[e] = running;
+  __syncthreads();
+  if (e == 0 && s_bad) flag_error(status, MOE_ERR_DEVICE_CHECK);
+  if (e < E) {
+    for (int b = 0; b < nb; ++b) blk_base[(size_t)b * E + e] += base;
+  }
+}
+
+__global__ void __launch_bounds__(PB) rank_kernel(const int32_t* __restrict__ topk_idx, int T,
+                                                  int k, int E,
+                                                  const int32_t* __restrict__ blk_base,
+                                                  int32_t* __restrict__ row_of_slot,
+                                                  int32_t* __restrict__ slot_of_row,
+                                                  int32_t* status) {
+  extern __shared__ uint32_t smem_u[];
+  uint32_t* masks = smem_u;
+  int32_t* sidx = reinterpret_cast<int32_t*>(smem_u + 8 * E);
+  const int b = blockIdx.x, t0 = b * PB;
+  build_masks(topk_idx, T, k, E, t0, masks, sidx, status);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tl = warp * 32 + lane;
+  const int t = t0 + tl;
+  if (t >= T) return;
+  const long long R = (long long)T * k;
+  const uint32_t below = (1u << lane) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const int e = sidx[tl * k + j];
+    const size_t s = (size_t)t * k + j;
+    if (e < 0 || e >= E) {
+      row_of_slot[s] = -1;
+      continue;
+    }
+    int rank = __popc(masks[warp * E + e] & below);
+    for (int w = 0; w < warp; ++w) rank += __popc(masks[w * E + e]);
+    const long long row = (long long)blk_base[(size_t)b * E + e] + rank;
+    if (row < 0 || row >= R) {
+      flag_error(status, MOE_ERR_DEVICE_CHECK);
+      row_of_slot[s] = -1;
+      continue;
+    }
+    row_of_slot[s] = (int32_t)row;
+    slot_of_row[row] = (int32_t)s;
+  }
+}
+
+// One warp per token: read the row once (16-byte vectors), write it to its k rows.
+__global__ void __launch_bounds__(256) copy_rows_kernel(const uint16_t* __restrict__ x,
+                                                        const int32_t* __restrict__ row_of_slot,
+                                                        int T, int H, int k,
+                                                        uint16_t* __restrict__ x_perm,
+                                                        int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const long long R = (long long)T * k;
+  int my_row = -1;
+  if (lane < k) {
+    const int r = row_of_slot[(size_t)t * k + lane];
+    if (r >= 0 && r < R) my_row = r;
+    else flag_error(status, MOE_ERR_DEVICE_CHECK);
+  }
+  const int nv = H / 8;  // 16-byte vectors per row
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  constexpr int U = 8;
+  for (int c0 = 0; c0 < nv; c0 += 32 * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * 32 + lane;
+      if (c < nv) v[u] = __ldg(src + c);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xFFFFFFFFu, my_row, j);
+      if (r < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * H);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < nv) dst[c] = v[u];
+      }
+    }
+  }
+}
+
+size_t mask_smem_bytes(int E, int k) { return (size_t)8 * E * 4 + (size_t)PB * k * 4; }
+
+}  // namespace
+
+cudaError_t launch_block_counts(const int32_t* topk_idx, int T, int k, int E, int32_t* blk_counts,
+                                int32_t* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int nb = (T + PB - 1) / PB;
+  block_counts_kernel<<<nb, PB, mask_smem_bytes(E, k), s>>>(topk_idx, T, k, E, blk_counts, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int32_t* blk_counts, int nb, int E, int R, int32_t* counts,
+                        int32_t* offsets, bool offsets_given, int32_t* blk_base, int32_t* status,
+                        cudaStream_t s) {
+  scan_kernel<<<1, kMaxE, 0, s>>>(blk_counts, nb, E, R, counts, offsets, offsets_given ? 1 : 0,
+                                  blk_base, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rank(const int32_t* topk_idx, int T, int k, int E, const int32_t* blk_base,
+                        int32_t* row_of_slot, int32_t* slot_of_row, int32_t* status,
+                        cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int nb = (T + PB - 1) / PB;
+  rank_kernel<<<nb, PB, mask_smem_bytes(E, k), s>>>(topk_idx, T, k, E, blk_base, row_of_slot,
+                                                    slot_of_row, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_rows(const void* x, const int32_t* row_of_slot, int T, int H, int k,
+                             void* x_perm, int32_t* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  copy_rows_kernel<<<(T + 7) / 8, 256, 0, s>>>(static_cast<const uint16_t*>(x), row_of_slot, T, H,
+                                              k, static_cast<uint16_t*>(x_perm), status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,64 @@
+// Internal launchers of the sm_103a kernels (one translation unit each); the
+// C ABI in moe_api.cu validates arguments and calls these.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 16;
+constexpr int kPermBlock = 256;  // tokens per ranking block of the permutation
+constexpr long long kSpinLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+// router: projection (FP32 FMA chain), softmax, top-k, renormalisation
+cudaError_t launch_route(const void* x, const float* w_router, const float* bias, int T, int H,
+                         int E, int k, int32_t* topk_idx, float* topk_w, cudaStream_t s);
+
+// per-block expert counts: blk_counts [nb, E], nb = ceil(T / kPermBlock)
+cudaError_t launch_block_counts(const int32_t* topk_idx, int T, int k, int E, int32_t* blk_counts,
+                                int32_t* status, cudaStream_t s);
+
+// counts [E] (nullable), offsets [E+1] (written, or read and checked if given),
+// blk_base [nb, E] = first row of each (block, expert)
+cudaError_t launch_scan(const int32_t* blk_counts, int nb, int E, int R, int32_t* counts,
+                        int32_t* offsets, bool offsets_given, int32_t* blk_base, int32_t* status,
+                        cudaStream_t s);
+
+// stable ranks: row_of_slot [T*k], slot_of_row [T*k]
+cudaError_t launch_rank(const int32_t* topk_idx, int T, int k, int E, const int32_t* blk_base,
+                        int32_t* row_of_slot, int32_t* slot_of_row, int32_t* status,
+                        cudaStream_t s);
+
+// x_perm[row_of_slot[t*k+j]] = x[t]
+cudaError_t launch_copy_rows(const void* x, const int32_t* row_of_slot, int T, int H, int k,
+                             void* x_perm, int32_t* status, cudaStream_t s);
+
+// packed weights: [E][2I][H] (gate/up interleaved in 128-row halves of 256-row
+// tiles) followed by [E][H][I] (down, transposed)
+cudaError_t launch_prepack(const void* w_gate, const void* w_up, const void* w_down, int E, int H,
+                           int I, void* packed, cudaStream_t s);
+
+// grouped GEMM-1 with the SwiGLU epilogue: h [R, I] bf16
+cudaError_t launch_gemm_gate_up(const CUtensorMap& a_xperm, const CUtensorMap& b_w1,
+                                const int32_t* offsets, int E, int R, int H, int I, void* h,
+                                int32_t* status, long long spin_limit, cudaStream_t s);
+
+// grouped GEMM-2: y [R, H] fp32
+cudaError_t launch_gemm_down(const CUtensorMap& a_h, const CUtensorMap& b_w2,
+                             const int32_t* offsets, int E, int R, int H, int I, float* y,
+                             int32_t* status, long long spin_limit, cudaStream_t s);
+
+// N tile width of the down projection for this H (fixed per model shape)
+int gemm_down_bn(int H);
+
+// out[t] = bf16(slot-order FMA chain of topk_w[t,j] * y[row_of_slot[t*k+j]])
+cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, int T,
+                           int H, int k, void* out, cudaStream_t s);
+
+// number of SMs of the current device (cached per device)
+int device_sm_count();
+
+}  // namespace moe

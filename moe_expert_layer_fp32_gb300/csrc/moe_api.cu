@@ -1,0 +1,407 @@
+// C ABI of the routed MoE layer forward (declared in include/moe.h): host-side
+// argument validation, the workspace layout, TMA tensor maps, and the launch
+// sequence route -> load stats -> permute -> grouped expert GEMMs -> combine.
+// No call allocates device memory or synchronises the stream (except
+// moe_read_device_status, whose job is to synchronise).
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+int device_sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 1;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+namespace {
+
+// ------------------------------------------------------------------ layout ---
+constexpr size_t kAlign = 256;
+inline size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t status, idx, w, counts, offsets, blk_counts, blk_base, row_of_slot, slot_of_row, x_perm,
+      h, y, total;
+};
+
+Layout layout(const moe_dims& d) {
+  const size_t T = (size_t)d.T, R = (size_t)d.T * d.k, E = (size_t)d.E;
+  const size_t nb = (T + kPermBlock - 1) / kPermBlock;
+  Layout L;
+  size_t o = 0;
+  L.status = o;       o += up(kAlign);
+  L.idx = o;          o += up(R * 4);
+  L.w = o;            o += up(R * 4);
+  L.counts = o;       o += up(E * 4);
+  L.offsets = o;      o += up((E + 1) * 4);
+  L.blk_counts = o;   o += up(nb * E * 4);
+  L.blk_base = o;     o += up(nb * E * 4);
+  L.row_of_slot = o;  o += up(R * 4);
+  L.slot_of_row = o;  o += up(R * 4);
+  L.x_perm = o;       o += up(R * (size_t)d.H * 2);
+  L.h = o;            o += up(R * (size_t)d.I * 2);
+  L.y = o;            o += up(R * (size_t)d.H * 4);
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+inline T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// -------------------------------------------------------------- validation ---
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_dims(const moe_dims& d) {
+  if (d.T < 0 || d.H <= 0 || d.E <= 0 || d.k <= 0 || d.I <= 0) return MOE_ERR_INVALID_ARG;
+  if (d.k > d.E) return MOE_ERR_INVALID_ARG;
+  if (d.E > kMaxE || d.k > kMaxK) return MOE_ERR_UNSUPPORTED;
+  if (d.H % 128 != 0 || d.I % 128 != 0 || d.H > 16384 || d.I > 16384) return MOE_ERR_UNSUPPORTED;
+  if ((long long)d.T * d.k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status need(const void* p) {
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+moe_status check_ws(const moe_dims& d, const void* ws, size_t ws_bytes) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < layout(d).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+#define MOE_TRY(expr)                 \
+  do {                                \
+    moe_status _s = (expr);           \
+    if (_s != MOE_OK) return _s;      \
+  } while (0)
+
+#define MOE_CUDA(expr)                          \
+  do {                                          \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+moe_status device_ok() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  static int cc_cache[64] = {};
+  int cc = dev < 64 ? cc_cache[dev] : 0;
+  if (cc == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    cc = major * 10 + minor;
+    if (dev < 64) cc_cache[dev] = cc;
+  }
+  return cc == 103 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------------------- tensor maps ---
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [outer, inner] row-major, box [box_outer, 64], 128-byte swizzle.
+moe_status make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                    uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return MOE_ERR_CUDA;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ step bodies ---
+moe_status do_load_stats(const int32_t* idx, const moe_dims& d, int32_t* counts,
+                         int32_t* offsets, bool offsets_given, void* ws, cudaStream_t s) {
+  const Layout L = layout(d);
+  const int nb = (d.T + kPermBlock - 1) / kPermBlock;
+  int32_t* status = at<int32_t>(ws, L.status);
+  MOE_CUDA(launch_block_counts(idx, d.T, d.k, d.E, at<int32_t>(ws, L.blk_counts), status, s));
+  MOE_CUDA(launch_scan(at<int32_t>(ws, L.blk_counts), nb, d.E, d.T * d.k, counts, offsets,
+                       offsets_given, at<int32_t>(ws, L.blk_base), status, s));
+  return MOE_OK;
+}
+
+moe_status do_permute_rows(const void* x, const int32_t* idx, const moe_dims& d, void* x_perm,
+                           int32_t* ros, int32_t* sor, void* ws, cudaStream_t s) {
+  const Layout L = layout(d);
+  int32_t* status = at<int32_t>(ws, L.status);
+  MOE_CUDA(launch_rank(idx, d.T, d.k, d.E, at<int32_t>(ws, L.blk_base), ros, sor, status, s));
+  MOE_CUDA(launch_copy_rows(x, ros, d.T, d.H, d.k, x_perm, status, s));
+  return MOE_OK;
+}
+
+moe_status do_expert_ffn(const void* x_perm, const int32_t* offsets, const void* packed,
+                         const moe_dims& d, float* y, void* ws, cudaStream_t s,
+                         cudaEvent_t after_gate_up = nullptr) {
+  const Layout L = layout(d);
+  const int R = d.T * d.k;
+  if (R == 0) return MOE_OK;
+  int32_t* status = at<int32_t>(ws, L.status);
+  void* h = at<void>(ws, L.h);
+  const uint16_t* w1 = static_cast<const uint16_t*>(packed);
+  const uint16_t* w2 = w1 + (size_t)d.E * 2 * d.I * d.H;
+  CUtensorMap ma, mb, mh, md;
+  MOE_TRY(make_map(&ma, x_perm, d.H, R, 128));
+  MOE_TRY(make_map(&mb, w1, d.H, (uint64_t)d.E * 2 * d.I, 256));
+  MOE_TRY(make_map(&mh, h, d.I, R, 128));
+  MOE_TRY(make_map(&md, w2, d.I, (uint64_t)d.E * d.H, gemm_down_bn(d.H)));
+  MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, d.E, R, d.H, d.I, h, status, kSpinLimitCycles, s));
+  if (after_gate_up != nullptr) MOE_CUDA(cudaEventRecord(after_gate_up, s));
+  MOE_CUDA(launch_gemm_down(mh, md, offsets, d.E, R, d.H, d.I, y, status, kSpinLimitCycles, s));
+  return MOE_OK;
+}
+
+moe_status layer_fwd(const void* x, const float* w_router, const float* bias,
+                     const void* packed_weights, const moe_dims& d, void* out,
+                     int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out,
+                     void* workspace, size_t ws_bytes, cudaStream_t s, cudaEvent_t* ev) {
+  MOE_TRY(check_dims(d));
+  MOE_TRY(check_ws(d, workspace, ws_bytes));
+  MOE_TRY(need(w_router));
+  if (bias != nullptr) MOE_TRY(need(bias));
+  MOE_TRY(need(packed_weights));
+  if (topk_idx_out != nullptr) MOE_TRY(need(topk_idx_out));
+  if (topk_w_out != nullptr) MOE_TRY(need(topk_w_out));
+  if (counts_out != nullptr) MOE_TRY(need(counts_out));
+  if (d.T > 0) {
+    MOE_TRY(need(x));
+    MOE_TRY(need(out));
+  }
+  MOE_TRY(device_ok());
+  const Layout L = layout(d);
+  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(workspace, L.idx);
+  float* w = topk_w_out ? topk_w_out : at<float>(workspace, L.w);
+  int32_t* counts = counts_out ? counts_out : at<int32_t>(workspace, L.counts);
+  int32_t* offsets = at<int32_t>(workspace, L.offsets);
+  int32_t* ros = at<int32_t>(workspace, L.row_of_slot);
+  int32_t* sor = at<int32_t>(workspace, L.slot_of_row);
+  void* x_perm = at<void>(workspace, L.x_perm);
+  float* y = at<float>(workspace, L.y);
+  auto mark = [&](int i) -> moe_status {
+    if (ev != nullptr && cudaEventRecord(ev[i], s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  };
+  MOE_TRY(mark(0));
+  MOE_CUDA(launch_route(x, w_router, bias, d.T, d.H, d.E, d.k, idx, w, s));
+  MOE_TRY(mark(1));
+  MOE_TRY(do_load_stats(idx, d, counts, offsets, false, workspace, s));
+  MOE_TRY(mark(2));
+  if (d.T > 0) MOE_TRY(do_permute_rows(x, idx, d, x_perm, ros, sor, workspace, s));
+  MOE_TRY(mark(3));
+  if (d.T > 0)
+    MOE_TRY(do_expert_ffn(x_perm, offsets, packed_weights, d, y, workspace, s,
+                          ev != nullptr ? ev[4] : nullptr));
+  else
+    MOE_TRY(mark(4));
+  MOE_TRY(mark(5));
+  if (d.T > 0) MOE_CUDA(launch_combine(y, w, ros, d.T, d.H, d.k, out, s));
+  MOE_TRY(mark(6));
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(moe_dims d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return layout(d).total;
+}
+
+size_t moe_packed_weight_bytes(moe_dims d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return (size_t)d.E * 3 * d.H * d.I * 2;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported dimensions or device";
+    case MOE_ERR_MISALIGNED: return "misaligned pointer";
+    case MOE_ERR_WORKSPACE: return "workspace or packed buffer too small";
+    case MOE_ERR_CUDA: return "CUDA runtime or launch error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side index or offset check failed";
+  }
+  return "unknown status";
+}
+
+moe_status moe_route(const void* x, const float* w_router, const float* bias, moe_dims d,
+                     int32_t* topk_idx, float* topk_w, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(need(x));
+  MOE_TRY(need(w_router));
+  if (bias != nullptr) MOE_TRY(need(bias));
+  MOE_TRY(need(topk_idx));
+  MOE_TRY(need(topk_w));
+  MOE_TRY(device_ok());
+  MOE_CUDA(launch_route(x, w_router, bias, d.T, d.H, d.E, d.k, topk_idx, topk_w, as_stream(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_load_stats(const int32_t* topk_idx, moe_dims d, int32_t* counts, int32_t* offsets,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T > 0) MOE_TRY(need(topk_idx));
+  MOE_TRY(need(counts));
+  MOE_TRY(need(offsets));
+  MOE_TRY(check_ws(d, workspace, ws_bytes));
+  MOE_TRY(device_ok());
+  return do_load_stats(topk_idx, d, counts, offsets, false, workspace, as_stream(stream));
+}
+
+moe_status moe_load_summary_host(const int32_t* counts_host, int32_t E, double* imbalance,
+                                 double* cv) {
+  if (counts_host == nullptr || E <= 0) return MOE_ERR_INVALID_ARG;
+  double sum = 0.0, mx = 0.0;
+  for (int e = 0; e < E; ++e) {
+    sum += counts_host[e];
+    mx = fmax(mx, (double)counts_host[e]);
+  }
+  const double mean = sum / E;
+  double var = 0.0;
+  for (int e = 0; e < E; ++e) var += (counts_host[e] - mean) * (counts_host[e] - mean);
+  var /= E;
+  if (imbalance) *imbalance = mean > 0 ? mx / mean - 1.0 : 0.0;
+  if (cv) *cv = mean > 0 ? sqrt(var) / mean : 0.0;
+  return MOE_OK;
+}
+
+moe_status moe_permute(const void* x, const int32_t* topk_idx, const int32_t* offsets, moe_dims d,
+                       void* x_perm, int32_t* row_of_slot, int32_t* slot_of_row, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(d));
+  MOE_TRY(need(offsets));
+  MOE_TRY(check_ws(d, workspace, ws_bytes));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(need(x));
+  MOE_TRY(need(topk_idx));
+  MOE_TRY(need(x_perm));
+  MOE_TRY(need(row_of_slot));
+  MOE_TRY(need(slot_of_row));
+  MOE_TRY(device_ok());
+  cudaStream_t s = as_stream(stream);
+  MOE_TRY(do_load_stats(topk_idx, d, nullptr, const_cast<int32_t*>(offsets), true, workspace, s));
+  return do_permute_rows(x, topk_idx, d, x_perm, row_of_slot, slot_of_row, workspace, s);
+}
+
+moe_status moe_prepack_expert_weights(const void* w_gate, const void* w_up, const void* w_down,
+                                      moe_dims d, void* packed, size_t packed_bytes,
+                                      void* stream) {
+  MOE_TRY(check_dims(d));
+  MOE_TRY(need(w_gate));
+  MOE_TRY(need(w_up));
+  MOE_TRY(need(w_down));
+  MOE_TRY(need(packed));
+  if (packed_bytes < moe_packed_weight_bytes(d)) return MOE_ERR_WORKSPACE;
+  MOE_TRY(device_ok());
+  MOE_CUDA(launch_prepack(w_gate, w_up, w_down, d.E, d.H, d.I, packed, as_stream(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void* packed_weights,
+                          moe_dims d, float* y, void* workspace, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(d));
+  MOE_TRY(check_ws(d, workspace, ws_bytes));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(need(x_perm));
+  MOE_TRY(need(offsets));
+  MOE_TRY(need(packed_weights));
+  MOE_TRY(need(y));
+  MOE_TRY(device_ok());
+  return do_expert_ffn(x_perm, offsets, packed_weights, d, y, workspace, as_stream(stream));
+}
+
+moe_status moe_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, moe_dims d,
+                       void* out, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(need(y));
+  MOE_TRY(need(topk_w));
+  MOE_TRY(need(row_of_slot));
+  MOE_TRY(need(out));
+  MOE_TRY(device_ok());
+  MOE_CUDA(launch_combine(y, topk_w, row_of_slot, d.T, d.H, d.k, out, as_stream(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_layer_fwd(const void* x, const float* w_router, const float* bias,
+                         const void* packed_weights, moe_dims d, void* out, int32_t* topk_idx_out,
+                         float* topk_w_out, int32_t* counts_out, void* workspace, size_t ws_bytes,
+                         void* stream) {
+  return layer_fwd(x, w_router, bias, packed_weights, d, out, topk_idx_out, topk_w_out, counts_out,
+                   workspace, ws_bytes, as_stream(stream), nullptr);
+}
+
+moe_status moe_layer_fwd_profiled(const void* x, const float* w_router, const float* bias,
+                                  const void* packed_weights, moe_dims d, void* out,
+                                  int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out,
+                                  void* workspace, size_t ws_bytes, void* stream,
+                                  void* const* events, int32_t n_events) {
+  if (n_events == 0 && events == nullptr)
+    return moe_layer_fwd(x, w_router, bias, packed_weights, d, out, topk_idx_out, topk_w_out,
+                         counts_out, workspace, ws_bytes, stream);
+  if (n_events != 7 || events == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaEvent_t ev[7];
+  for (int i = 0; i < 7; ++i) {
+    if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+    ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  return layer_fwd(x, w_router, bias, packed_weights, d, out, topk_idx_out, topk_w_out, counts_out,
+                   workspace, ws_bytes, as_stream(stream), ev);
+}
+
+moe_status moe_read_device_status(void* workspace, int32_t* status_out, void* stream) {
+  if (workspace == nullptr || status_out == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return MOE_ERR_MISALIGNED;
+  cudaStream_t s = as_stream(stream);
+  int32_t v = 0;
+  MOE_CUDA(cudaMemcpyAsync(&v, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  MOE_CUDA(cudaMemsetAsync(workspace, 0, sizeof(int32_t), s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  *status_out = v;
+  return MOE_OK;
+}
+
+}  // extern "C"

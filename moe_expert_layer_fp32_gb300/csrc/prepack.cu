@@ -1,0 +1,65 @@
+// One-time expert-weight preparation: logical row-major weights -> the K-major
+// layouts the grouped GEMMs stream with TMA.
+//
+//   W1 [E][2I][H]: for N-tile n (256 rows), rows 0..127 are gate columns
+//                  128n..128n+127 and rows 128..255 the matching up columns, each
+//                  stored as a row over h (K-major).  One MMA tile then holds a
+//                  gate block and its up block, so SwiGLU runs in the epilogue.
+//   W2 [E][H][I]:  row c is down-projection column c over i (K-major).
+//
+// 32x32 tiles through shared memory; reads and writes are both coalesced.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+// src: per expert a [rows x cols] row-major matrix.  Writes dst[(e, map(col)), row].
+// mode 0: gate half of W1, mode 1: up half of W1, mode 2: W2.
+__global__ void __launch_bounds__(256) transpose_pack_kernel(const uint16_t* __restrict__ src,
+                                                             int rows, int cols, int mode, int I,
+                                                             int H, uint16_t* __restrict__ dst) {
+  __shared__ uint16_t tile[32][33];
+  const int e = blockIdx.z;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const uint16_t* s = src + (size_t)e * rows * cols;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = s[(size_t)r * cols + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i;          // source column -> destination row
+    const int r = r0 + threadIdx.x;  // source row -> destination column
+    if (r >= rows || c >= cols) continue;
+    size_t drow;
+    int dld;
+    if (mode < 2) {
+      drow = (size_t)e * 2 * I + (size_t)(c / 128) * 256 + (c % 128) + (mode == 1 ? 128 : 0);
+      dld = H;
+    } else {
+      drow = (size_t)e * H + c;
+      dld = I;
+    }
+    dst[drow * dld + r] = tile[threadIdx.x][i];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prepack(const void* w_gate, const void* w_up, const void* w_down, int E, int H,
+                           int I, void* packed, cudaStream_t s) {
+  uint16_t* w1 = static_cast<uint16_t*>(packed);
+  uint16_t* w2 = w1 + (size_t)E * 2 * I * H;
+  dim3 block(32, 8);
+  dim3 g1((I + 31) / 32, (H + 31) / 32, E);  // gate/up: [H x I] per expert
+  transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_gate), H, I, 0, I, H,
+                                             w1);
+  transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_up), H, I, 1, I, H, w1);
+  dim3 g2((H + 31) / 32, (I + 31) / 32, E);  // down: [I x H] per expert
+  transpose_pack_kernel<<<g2, block, 0, s>>>(static_cast<const uint16_t*>(w_down), I, H, 2, I, H,
+                                             w2);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -31,10 +31,11 @@ def build(force: bool = False) -> str:
     """Compile liboracle.so next to its source (g++, no CUDA, no contraction)."""
     with _lock:
         if (not force and os.path.exists(_LIB_PATH)
-                and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+                and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
+                                                        os.path.getmtime(__file__))):
             return _LIB_PATH
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared",
+        subprocess.check_call(["g++", "-O3", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared",
                                "-pthread", _SRC, "-o", tmp])
         os.replace(tmp, _LIB_PATH)
         return _LIB_PATH

@@ -45,7 +45,8 @@ def build(force: bool = False) -> str:
     """Compile libsynth.so next to its source (gcc, no CUDA)."""
     with _lock:
         if (not force and os.path.exists(_LIB_PATH)
-                and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+                and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
+                                                        os.path.getmtime(__file__))):
             return _LIB_PATH
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
