@@ -173,10 +173,12 @@ def oracle_sample(wl, x, wr, bias, host_w, S):
 
 
 def calibrate_sample(wl, x, wr, bias, host_w, target_s):
-    S = min(wl.T, 8)
+    """Token count whose oracle run takes about target_s seconds (two probes: the
+    first also warms page caches and thread start-up)."""
+    oracle_sample(wl, x, wr, bias, host_w, min(wl.T, 8))
+    S = min(wl.T, 32)
     t = oracle_sample(wl, x, wr, bias, host_w, S)
-    S = int(max(8, min(wl.T, S * target_s / max(t, 1e-3))))
-    return S
+    return int(max(8, min(wl.T, S * target_s / max(t, 1e-3))))
 
 
 def host_weight_fn(wl, full=None):

@@ -172,6 +172,9 @@ def moe_layer_fwd_profiled(x, w_router, bias, packed_weights, d, out, topk_idx_o
     boundaries (before route, after route, load stats, permute, gate/up GEMM,
     down GEMM, combine)."""
     wp, wb = _ws(workspace)
+    for e in events:
+        if e.cuda_event == 0:  # torch creates the CUDA event on its first record
+            e.record(torch.cuda.current_stream() if stream is None else stream)
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check("moe_layer_fwd_profiled", _lib.moe_layer_fwd_profiled(
         _ptr(x), _ptr(w_router), _ptr(bias), _ptr(packed_weights), d, _ptr(out),
