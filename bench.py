@@ -154,22 +154,25 @@ def workload_config(wl, world, l2_note):
 
 # ------------------------------------------------------------ CPU oracle ---
 def oracle_sample(wl, x, wr, bias, host_w, S):
-    """Runs the oracle's steps on the first S tokens; returns seconds.  Expert
-    weights are restricted to the experts those tokens use (every row's work is
-    unchanged; only untouched experts are left out)."""
+    """Runs the oracle's steps on the first S tokens; returns the seconds spent in
+    oracle calls.  Expert weights are restricted to the experts those tokens use
+    (every row's work is unchanged; only untouched experts are left out), and
+    gathering them is not timed."""
     import oracle
     t0 = time.perf_counter()
     idx, w = oracle.route(x[:S], wr, bias, wl.k)
+    t_route = time.perf_counter() - t0
     experts = np.unique(idx)
     remap = np.full(wl.E, -1, np.int64)
     remap[experts] = np.arange(len(experts))
     sub_idx = remap[idx].astype(np.int32)
+    wg, wu, wd = host_w(experts)
+    t1 = time.perf_counter()
     counts, offsets, _, _ = oracle.load_stats(sub_idx, len(experts))
     xp, ros, _ = oracle.permute(x[:S], sub_idx, offsets, len(experts))
-    wg, wu, wd = host_w(experts)
     y = oracle.expert_ffn(xp, offsets, wg, wu, wd)
     oracle.combine(y, w, ros)
-    return time.perf_counter() - t0
+    return t_route + time.perf_counter() - t1
 
 
 def calibrate_sample(wl, x, wr, bias, host_w, target_s):
