@@ -180,6 +180,29 @@ moe_status moe_layer_fwd_profiled(const void* x, const float* w_router, const fl
                                   void* workspace, size_t ws_bytes, void* stream,
                                   void* const* events, int32_t n_events);
 
+/* moe_load_stats for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point: it exists for callers that run where
+ * calling cudaMalloc (or taking memory from an allocator) is not allowed, such as
+ * code inside a host framework whose device memory is owned by its own pool, or
+ * a serving loop that must not allocate after start-up because an allocation can
+ * synchronise the device.  It computes exactly what moe_load_stats computes
+ * (counts [E], offsets [E+1]) from the same inputs, but keeps the per-block
+ * partial counts in a 2 MiB scratch array compiled into the library (one per GPU
+ * that loads it, held until the process exits) instead of a caller workspace.
+ *   Limit: 2 * ceil(T / 256) * E <= 524288 (for E = 256: T <= 262144); larger
+ *   sizes return MOE_ERR_UNSUPPORTED before anything is launched.
+ *   device_status: optional device int32 (NULL: not reported); receives
+ *   MOE_ERR_DEVICE_CHECK if an expert id is out of range or repeated within a
+ *   token (the caller zeroes it beforehand).
+ * The first call on each device looks up the scratch array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.  All
+ * calls on a device share the one scratch array, and each call overwrites the
+ * part of it that it reads, so calls whose kernels can overlap on the GPU (other
+ * streams, other host threads) race: serialise them.  Nothing is allocated or
+ * freed. */
+moe_status moe_load_stats_noalloc(const int32_t* topk_idx, moe_dims d, int32_t* counts,
+                                  int32_t* offsets, int32_t* device_status, void* stream);
+
 /* Synchronises `stream`, returns the workspace status word in *status_out
  * (MOE_OK or the first device-side error recorded since the last read) and
  * clears it. */

@@ -32,7 +32,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 ABI_SYMBOLS = ("moe_workspace_bytes", "moe_packed_weight_bytes", "moe_route", "moe_load_stats",
                "moe_load_summary_host", "moe_permute", "moe_prepack_expert_weights",
                "moe_expert_ffn", "moe_combine", "moe_layer_fwd", "moe_layer_fwd_profiled",
-               "moe_read_device_status", "moe_status_string")
+               "moe_read_device_status", "moe_status_string", "moe_load_stats_noalloc")
 
 
 class moe_dims(ctypes.Structure):
@@ -64,6 +64,7 @@ _sig = {
                                               _vp, _sz, _vp, _vp, _i32]),
     "moe_read_device_status": (ctypes.c_int, [_vp, _vp, _vp]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_load_stats_noalloc": (ctypes.c_int, [_vp, moe_dims, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -122,6 +123,14 @@ def moe_load_stats(topk_idx, d, counts, offsets, workspace, stream=None):
     wp, wb = _ws(workspace)
     _check("moe_load_stats", _lib.moe_load_stats(_ptr(topk_idx), d, _ptr(counts), _ptr(offsets),
                                                  wp, wb, _stream(stream)))
+
+
+def moe_load_stats_noalloc(topk_idx, d, counts, offsets, device_status=None, stream=None):
+    """moe_load_stats without a workspace, for callers that cannot allocate: the
+    library's own fixed scratch array holds the partial counts (see include/moe.h
+    for the size limit and the rule that overlapping calls race)."""
+    _check("moe_load_stats_noalloc", _lib.moe_load_stats_noalloc(
+        _ptr(topk_idx), d, _ptr(counts), _ptr(offsets), _ptr(device_status), _stream(stream)))
 
 
 def moe_load_summary_host(counts_host):
