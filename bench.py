@@ -52,7 +52,25 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="override T of the workload (smaller cases for profiling)")
+    p.add_argument("--experts", type=int, default=None,
+                   help="override E of the workload (smaller cases for profiling)")
     return p.parse_args()
+
+
+def chosen_workload(args):
+    import dataclasses
+    wl = synth.WORKLOADS[args.workload]
+    changes = {}
+    if args.tokens is not None:
+        changes["T"] = args.tokens
+    if args.experts is not None:
+        changes["E"] = args.experts
+    if changes:
+        tag = ",".join(f"{k}={v}" for k, v in changes.items())
+        wl = dataclasses.replace(wl, name=f"{wl.name}[{tag}]", **changes)
+    return wl
 
 
 # ------------------------------------------------------------ distributed ---
@@ -195,7 +213,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    wl = synth.WORKLOADS[args.workload]
+    wl = chosen_workload(args)
     x = synth.tokens(wl)
     wr, bias = synth.router(wl)
     host_w = host_weight_fn(wl)
@@ -227,7 +245,7 @@ def run_ours(args):
     dist = dist_init(world, True)
     import moe_expert_layer_fp32_gb300 as moe
 
-    wl = synth.WORKLOADS[args.workload]
+    wl = chosen_workload(args)
     T, H, E, k, I = wl.T, wl.H, wl.E, wl.k, wl.I
     R = T * k
     d = moe.dims(T, H, E, k, I)

@@ -51,7 +51,10 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int NBAR = 2 * STAGES + 2 + 2 + 1;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NBAR * 8 + 16 +
+  // epilogue staging: per epilogue warp a 32 x 32-word tile (row stride 36 words)
+  static constexpr int EPI_LD = 36;
+  static constexpr int EPI_BYTES = 4 * 32 * EPI_LD * 4;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NBAR * 8 + 16 +
                                     2 * (kMaxE + 1) * 4;
 };
 
@@ -87,6 +90,28 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long 
 
 __device__ __forceinline__ float silu_f32(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
 
+// One warp writes a 32-row x 128-byte block whose row i (i = lane) it holds in
+// registers: the rows go through shared memory so that every global store
+// instruction writes four whole 128-byte row segments instead of 32 scattered
+// 16-byte pieces.  Row r of the block goes to dst + r * ld_bytes; rows >= nrows
+// are skipped.
+__device__ __forceinline__ void store_rows_128b(const uint32_t (&w)[32], uint32_t* stile, int lane,
+                                                uint8_t* dst, size_t ld_bytes, int nrows) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    *reinterpret_cast<uint4*>(stile + lane * 36 + 4 * q) =
+        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  __syncwarp();
+  const int cb = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    const uint4 v = *reinterpret_cast<const uint4*>(stile + r * 36 + 4 * cb);
+    if (r < nrows) *reinterpret_cast<uint4*>(dst + r * ld_bytes + 16 * cb) = v;
+  }
+  __syncwarp();
+}
+
 template <int BN, bool SWIGLU>
 __global__ void __launch_bounds__(192, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -100,7 +125,8 @@ __global__ void __launch_bounds__(192, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = base;
   uint8_t* sB = base + C::STAGES * C::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  uint32_t* s_epi = reinterpret_cast<uint32_t*>(sB + C::STAGES * C::B_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s_epi) + C::EPI_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* tfull = bars + 2 * C::STAGES;
@@ -222,7 +248,6 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row_in_tile = q * 32 + lane;
     int tcount = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
       const Tile ti = decode_tile(t, s_prefix, s_off, E, NT);
@@ -234,45 +259,43 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      const bool valid = row_in_tile < ti.rows;
-      const size_t grow = (size_t)(ti.a_row0 + row_in_tile);
+      // rows of this warp's 32-row block that belong to the tile's expert
+      const int nrows = min(32, max(0, ti.rows - q * 32));
+      uint32_t* stile = s_epi + q * 32 * C::EPI_LD;
       if constexpr (SWIGLU) {
-        // accumulator columns [0, BN/2) = gate, [BN/2, BN) = up, same intermediate index
-        uint16_t* hrow = static_cast<uint16_t*>(out) + grow * out_ld + ti.nt * (BN / 2);
+        // accumulator columns [0, BN/2) = gate, [BN/2, BN) = up, same intermediate index;
+        // 64 intermediate columns (128 bytes of h per row) per pass
+        uint8_t* dst = static_cast<uint8_t*>(out) +
+                       ((size_t)(ti.a_row0 + q * 32) * out_ld + ti.nt * (BN / 2)) * 2;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld_32x32b_x32(taddr + c0, g);
-          tmem_ld_32x32b_x32(taddr + BN / 2 + c0, u);
-          tmem_ld_wait();
-          uint32_t hp[16];
+        for (int c0 = 0; c0 < BN / 2; c0 += 64) {
+          uint32_t hp[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float h0 = __fmul_rn(silu_f32(__uint_as_float(g[2 * i])), __uint_as_float(u[2 * i]));
-            const float h1 =
-                __fmul_rn(silu_f32(__uint_as_float(g[2 * i + 1])), __uint_as_float(u[2 * i + 1]));
-            hp[i] = pack_bf16x2(h0, h1);
-          }
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(hrow + c0);
+          for (int half = 0; half < 2; ++half) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(taddr + c0 + 32 * half, g);
+            tmem_ld_32x32b_x32(taddr + BN / 2 + c0 + 32 * half, u);
+            tmem_ld_wait();
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(hp[4 * v], hp[4 * v + 1], hp[4 * v + 2], hp[4 * v + 3]);
+            for (int i = 0; i < 16; ++i) {
+              const float h0 =
+                  __fmul_rn(silu_f32(__uint_as_float(g[2 * i])), __uint_as_float(u[2 * i]));
+              const float h1 = __fmul_rn(silu_f32(__uint_as_float(g[2 * i + 1])),
+                                         __uint_as_float(u[2 * i + 1]));
+              hp[16 * half + i] = pack_bf16x2(h0, h1);
+            }
           }
+          store_rows_128b(hp, stile, lane, dst + c0 * 2, (size_t)out_ld * 2, nrows);
         }
       } else {
-        float* yrow = static_cast<float*>(out) + grow * out_ld + ti.nt * BN;
+        uint8_t* dst = static_cast<uint8_t*>(out) +
+                       ((size_t)(ti.a_row0 + q * 32) * out_ld + ti.nt * BN) * 4;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + c0, v);
           tmem_ld_wait();
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(yrow + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          }
+          store_rows_128b(v, stile, lane, dst + c0 * 4, (size_t)out_ld * 4, nrows);
         }
       }
       tc_fence_before();
