@@ -9,30 +9,45 @@
 //   GEMM-1 (gate/up, SwiGLU epilogue): h[r, :] = bf16(silu(x_perm[r] Wg_e) * (x_perm[r] Wu_e))
 //   GEMM-2 (down):                     y[r, :] = h[r] Wd_e            (FP32 out)
 //
-// Design (one persistent CTA per SM, 192 threads, warp-specialised):
+// Design (persistent CTAs, one per SM, 192 threads, warp-specialised):
 //   warp 0 lane 0   TMA producer: 128x64 A tile + BNx64 B tile per stage into a
 //                   STAGES-deep ring of 128-byte-swizzled shared-memory buffers.
 //   warp 1 lane 0   MMA issuer: tcgen05.mma kind::f16, M=128, N=BN, K=16, four
 //                   per 64-wide k-block, accumulating in TMEM; tcgen05.commit
 //                   frees each stage and signals a finished accumulator.
 //   warps 2..5      epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
-//                   SwiGLU or FP32 pass-through, 16-byte global stores of the
-//                   rows that belong to the tile's expert.
+//                   SwiGLU or FP32 pass-through, rows staged through shared
+//                   memory so every global store writes whole 128-byte segments.
 // Two TMEM accumulators (2*BN columns) let the epilogue of tile i overlap the
 // main loop of tile i+1.
 //
-// Tiles: for each expert e, ceil(M_e/128) row tiles x (N/BN) column tiles,
-// numbered expert-major, row-tile, column-tile; CTA c takes tiles c, c+grid, ...
-// The schedule is built on the device from `offsets`, so no host round trip.
-// A row tile may run past its expert's last row into the next expert's rows or
-// past the end (TMA fills zeros there); those rows are computed but never
-// stored, and a row's result does not depend on the other rows of its tile.
+// Tiles: for each expert e, ceil(M_e/128) row tiles x (N/BN) column tiles, built
+// on the device from `offsets` (no host round trip).  A row tile may run past
+// its expert's last row into the next expert's rows or past the end (TMA fills
+// zeros there); those rows are computed but never stored, and a row's result
+// does not depend on the other rows of its tile.
+//
+// CL = 2 (used when N/BN is even): CTAs work in clusters of two that split the
+// L2->SM traffic of a pair of tiles sharing an operand.  Work units, numbered
+// expert-major:
+//   "B-shared": row tiles 2p and 2p+1 of expert e with the same column tile; each
+//               CTA loads its own A tile and one half of the B tile, multicast
+//               to both CTAs;
+//   "A-shared": an expert's odd last row tile with column tiles 2j and 2j+1;
+//               each CTA loads its own B tile and one half of the A tile,
+//               multicast to both.
+// Either way each CTA's stage still holds a full A and B tile and runs the same
+// cta_group::1 MMAs, so the arithmetic is unchanged; a stage is refilled only
+// after both CTAs' MMAs have released it (multicast commit, 2 arrivals).
+// CL = 1: every CTA loads its own tiles (odd N/BN).
+//
 // The tile shape, K order (k-blocks ascending, 16-wide MMAs ascending) and N
 // split depend only on H and I, never on T: batch-invariant by construction.
 //
 // Every wait is bounded (clock64 limit); a wait that runs out raises a CTA-wide
 // abort flag and records MOE_ERR_TIMEOUT; the roles then drain their own
-// in-flight TMA copies and MMAs (bounded again) before TMEM is released.
+// in-flight TMA copies and MMAs (bounded again) before TMEM is released, and
+// the two CTAs of a cluster meet at a cluster barrier before either exits.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -55,30 +70,61 @@ struct Cfg {
   static constexpr int EPI_LD = 36;
   static constexpr int EPI_BYTES = 4 * 32 * EPI_LD * 4;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NBAR * 8 + 16 +
-                                    2 * (kMaxE + 1) * 4;
+                                    3 * (kMaxE + 1) * 4;
 };
 
-struct Tile {
-  int e, nt, a_row0, rows;
+// Tensor maps of one grouped GEMM: A (rows of x_perm or h) in boxes of 128 and
+// 64 rows, B (packed weight rows) in boxes of BN and BN/2 rows; all 64 columns.
+struct Maps {
+  CUtensorMap a128, a64, b_full, b_half;
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const int* s_prefix, const int* s_off, int E,
-                                            int NT) {
-  // largest e with s_prefix[e] <= t (experts without tiles share the next prefix)
+// One CTA's share of a work unit.
+struct Work {
+  int e, nt;       // expert, this CTA's column tile
+  int a_row0;      // first row of this CTA's row tile
+  int rows;        // rows of the tile that belong to expert e
+  int mode;        // 0: own tiles, 1: B-shared, 2: A-shared
+  int a_load_row;  // first row of the A box this CTA issues
+  int b_load_row;  // first row of the B box this CTA issues
+};
+
+template <int BN, int CL>
+__device__ __forceinline__ Work decode(int u, int rank, const int* s_prefix, const int* s_off,
+                                       const int* s_mt, int E, int NT, int n_per_expert) {
+  // largest e with s_prefix[e] <= u (experts without work share the next prefix)
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s_prefix[mid] <= t) lo = mid;
+    if (s_prefix[mid] <= u) lo = mid;
     else hi = mid - 1;
   }
-  const int local = t - s_prefix[lo];
-  const int mt = local / NT;
-  Tile ti;
-  ti.e = lo;
-  ti.nt = local - mt * NT;
-  ti.a_row0 = s_off[lo] + mt * GM;
-  ti.rows = min(GM, s_off[lo + 1] - ti.a_row0);
-  return ti;
+  const int local = u - s_prefix[lo];
+  Work w;
+  w.e = lo;
+  int mt;
+  if constexpr (CL == 1) {
+    mt = local / NT;
+    w.nt = local - mt * NT;
+    w.mode = 0;
+  } else {
+    const int nB = (s_mt[lo] >> 1) * NT;
+    if (local < nB) {
+      const int mp = local / NT;
+      w.nt = local - mp * NT;
+      mt = 2 * mp + rank;
+      w.mode = 1;
+    } else {
+      mt = s_mt[lo] - 1;
+      w.nt = 2 * (local - nB) + rank;
+      w.mode = 2;
+    }
+  }
+  w.a_row0 = s_off[lo] + mt * GM;
+  w.rows = min(GM, s_off[lo + 1] - w.a_row0);
+  w.a_load_row = w.a_row0 + (w.mode == 2 ? rank * (GM / 2) : 0);
+  w.b_load_row = lo * n_per_expert + w.nt * BN + (w.mode == 1 ? rank * (BN / 2) : 0);
+  return w;
 }
 
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long long limit) {
@@ -112,13 +158,11 @@ __device__ __forceinline__ void store_rows_128b(const uint32_t (&w)[32], uint32_
   __syncwarp();
 }
 
-template <int BN, bool SWIGLU>
+template <int BN, bool SWIGLU, int CL>
 __global__ void __launch_bounds__(192, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB,
-                        const int32_t* __restrict__ offsets, int E, int R, int n_per_expert, int K,
-                        void* __restrict__ out, int out_ld, int32_t* status,
-                        long long spin_limit) {
+    grouped_gemm_kernel(const __grid_constant__ Maps maps, const int32_t* __restrict__ offsets,
+                        int E, int R, int n_per_expert, int K, void* __restrict__ out, int out_ld,
+                        int32_t* status, long long spin_limit) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -136,21 +180,26 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_off = s_prefix + (kMaxE + 1);
+  int* s_mt = s_off + (kMaxE + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = n_per_expert / BN;
   const int KB = K / GK;
+  const int rank = (CL == 2) ? (int)cluster_ctarank() : 0;
+  const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
 
   if (threadIdx.x == 0) {
-    // schedule: validate offsets (0 = o_0 <= o_1 <= ... <= o_E = R), tile prefix
+    // schedule: validate offsets (0 = o_0 <= o_1 <= ... <= o_E = R), work prefix
     bool ok = __ldg(offsets) == 0 && __ldg(offsets + E) == R;
     int p = 0;
     for (int e = 0; e < E; ++e) {
       const int a = __ldg(offsets + e), b = __ldg(offsets + e + 1);
       if (b < a) ok = false;
+      const int mt = b > a ? (b - a + GM - 1) / GM : 0;
       s_off[e] = a;
+      s_mt[e] = mt;
       s_prefix[e] = p;
-      if (b > a) p += ((b - a + GM - 1) / GM) * NT;
+      p += mt * NT / CL;  // CL == 2 only when NT is even
     }
     s_off[E] = __ldg(offsets + E);
     if (!ok) {
@@ -162,7 +211,7 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CL);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -172,12 +221,17 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&tmA);
-    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&maps.a128);
+    prefetch_tensormap(&maps.b_full);
+    if constexpr (CL == 2) {
+      prefetch_tensormap(&maps.a64);
+      prefetch_tensormap(&maps.b_half);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
+  if constexpr (CL == 2) cluster_sync();  // the peer's barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = s_prefix[E];
@@ -187,9 +241,8 @@ __global__ void __launch_bounds__(192, 1)
       // ------------------------------------------------------------ producer
       int it = 0;  // k-blocks issued
       bool aborted = false;
-      for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
-        const Tile ti = decode_tile(t, s_prefix, s_off, E, NT);
-        const int b_row0 = ti.e * n_per_expert + ti.nt * BN;
+      for (int u = unit0; u < total && !aborted; u += unit_step) {
+        const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, n_per_expert);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -198,8 +251,20 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-          tma_load_2d(&tmA, sA + s * C::A_BYTES, &full[s], kb * GK, ti.a_row0);
-          tma_load_2d(&tmB, sB + s * C::B_BYTES, &full[s], kb * GK, b_row0);
+          uint8_t* a_dst = sA + s * C::A_BYTES;
+          uint8_t* b_dst = sB + s * C::B_BYTES;
+          if (w.mode == 2) {
+            tma_load_2d_multicast(&maps.a64, a_dst + rank * (GM / 2) * 128, &full[s], kb * GK,
+                                  w.a_load_row, 0x3);
+          } else {
+            tma_load_2d(&maps.a128, a_dst, &full[s], kb * GK, w.a_load_row);
+          }
+          if (w.mode == 1) {
+            tma_load_2d_multicast(&maps.b_half, b_dst + rank * (BN / 2) * 128, &full[s], kb * GK,
+                                  w.b_load_row, 0x3);
+          } else {
+            tma_load_2d(&maps.b_full, b_dst, &full[s], kb * GK, w.b_load_row);
+          }
         }
       }
       if (aborted) {
@@ -213,7 +278,7 @@ __global__ void __launch_bounds__(192, 1)
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t IDESC = idesc_bf16_f32(GM, BN);
       int it = 0, tcount = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+      for (int u = unit0; u < total; u += unit_step, ++tcount) {
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (!mbar_wait_bounded(&tempty[acc], aph ^ 1, abort_flag, status, spin_limit)) break;
@@ -236,7 +301,8 @@ __global__ void __launch_bounds__(192, 1)
                      sdesc_k_major_sw128(b_addr + kk * UK * 2), IDESC,
                      (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&empty[s]);
+          if constexpr (CL == 2) mma_commit_multicast(&empty[s], 0x3);
+          else mma_commit(&empty[s]);
         }
         if (aborted) break;
         mma_commit(&tfull[acc]);
@@ -249,8 +315,8 @@ __global__ void __launch_bounds__(192, 1)
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int tcount = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
-      const Tile ti = decode_tile(t, s_prefix, s_off, E, NT);
+    for (int u = unit0; u < total; u += unit_step, ++tcount) {
+      const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, n_per_expert);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       int ok = 1;
@@ -260,28 +326,28 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       // rows of this warp's 32-row block that belong to the tile's expert
-      const int nrows = min(32, max(0, ti.rows - q * 32));
+      const int nrows = min(32, max(0, w.rows - q * 32));
       uint32_t* stile = s_epi + q * 32 * C::EPI_LD;
       if constexpr (SWIGLU) {
         // accumulator columns [0, BN/2) = gate, [BN/2, BN) = up, same intermediate index;
         // 64 intermediate columns (128 bytes of h per row) per pass
         uint8_t* dst = static_cast<uint8_t*>(out) +
-                       ((size_t)(ti.a_row0 + q * 32) * out_ld + ti.nt * (BN / 2)) * 2;
+                       ((size_t)(w.a_row0 + q * 32) * out_ld + w.nt * (BN / 2)) * 2;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN / 2; c0 += 64) {
           uint32_t hp[32];
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            uint32_t g[32], u[32];
+            uint32_t g[32], uu[32];
             tmem_ld_32x32b_x32(taddr + c0 + 32 * half, g);
-            tmem_ld_32x32b_x32(taddr + BN / 2 + c0 + 32 * half, u);
+            tmem_ld_32x32b_x32(taddr + BN / 2 + c0 + 32 * half, uu);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float h0 =
-                  __fmul_rn(silu_f32(__uint_as_float(g[2 * i])), __uint_as_float(u[2 * i]));
+                  __fmul_rn(silu_f32(__uint_as_float(g[2 * i])), __uint_as_float(uu[2 * i]));
               const float h1 = __fmul_rn(silu_f32(__uint_as_float(g[2 * i + 1])),
-                                         __uint_as_float(u[2 * i + 1]));
+                                         __uint_as_float(uu[2 * i + 1]));
               hp[16 * half + i] = pack_bf16x2(h0, h1);
             }
           }
@@ -289,7 +355,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       } else {
         uint8_t* dst = static_cast<uint8_t*>(out) +
-                       ((size_t)(ti.a_row0 + q * 32) * out_ld + ti.nt * BN) * 4;
+                       ((size_t)(w.a_row0 + q * 32) * out_ld + w.nt * BN) * 4;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t v[32];
@@ -305,52 +371,115 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CL == 2) cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
-template <int BN, bool SWIGLU>
-cudaError_t launch_grouped(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets,
-                           int E, int R, int n_per_expert, int K, void* out, int out_ld,
-                           int32_t* status, long long spin_limit, cudaStream_t s) {
+// Per device and kernel: the shared-memory opt-in and the grid (SMs, or twice
+// the number of co-resident two-CTA clusters).
+template <int BN, bool SWIGLU, int CL>
+cudaError_t kernel_grid(int* grid) {
   using C = Cfg<BN>;
-  static bool attr_set[64] = {};
+  static int cache[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 64 && !attr_set[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<BN, SWIGLU>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
+  if (dev < 64 && cache[dev] > 0) {
+    *grid = cache[dev];
+    return cudaSuccess;
   }
-  const int grid = device_sm_count();
-  grouped_gemm_kernel<BN, SWIGLU><<<grid, 192, C::SMEM_BYTES, s>>>(
-      a, b, offsets, E, R, n_per_expert, K, out, out_ld, status, spin_limit);
-  return cudaGetLastError();
+  auto kern = grouped_gemm_kernel<BN, SWIGLU, CL>;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  int g = device_sm_count();
+  if constexpr (CL == 2) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * g, 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (err != cudaSuccess) return err;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    g = 2 * clusters;
+  }
+  if (dev < 64) cache[dev] = g;
+  *grid = g;
+  return cudaSuccess;
+}
+
+template <int BN, bool SWIGLU, int CL>
+cudaError_t launch_grouped(const Maps& maps, const int32_t* offsets, int E, int R,
+                           int n_per_expert, int K, void* out, int out_ld, int32_t* status,
+                           long long spin_limit, cudaStream_t s) {
+  using C = Cfg<BN>;
+  int grid = 0;
+  cudaError_t err = kernel_grid<BN, SWIGLU, CL>(&grid);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  if constexpr (CL == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<BN, SWIGLU, CL>, maps, offsets, E, R,
+                            n_per_expert, K, out, out_ld, status, spin_limit);
 }
 
 }  // namespace
 
 int gemm_down_bn(int H) { return (H % 256 == 0) ? 256 : 128; }
 
-cudaError_t launch_gemm_gate_up(const CUtensorMap& a_xperm, const CUtensorMap& b_w1,
-                                const int32_t* offsets, int E, int R, int H, int I, void* h,
-                                int32_t* status, long long spin_limit, cudaStream_t s) {
+cudaError_t launch_gemm_gate_up(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets,
+                                int E, int R, int H, int I, void* h, int32_t* status,
+                                long long spin_limit, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
-  return launch_grouped<256, true>(a_xperm, b_w1, offsets, E, R, 2 * I, H, h, I, status,
-                                   spin_limit, s);
+  Maps m;
+  if (!a.encode(&m.a128, 128) || !a.encode(&m.a64, 64) || !b.encode(&m.b_full, 256) ||
+      !b.encode(&m.b_half, 128))
+    return cudaErrorInvalidValue;
+  const int NT = (2 * I) / 256;
+  if (NT % 2 == 0)
+    return launch_grouped<256, true, 2>(m, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s);
+  return launch_grouped<256, true, 1>(m, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s);
 }
 
-cudaError_t launch_gemm_down(const CUtensorMap& a_h, const CUtensorMap& b_w2,
-                             const int32_t* offsets, int E, int R, int H, int I, float* y,
-                             int32_t* status, long long spin_limit, cudaStream_t s) {
+cudaError_t launch_gemm_down(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets,
+                             int E, int R, int H, int I, float* y, int32_t* status,
+                             long long spin_limit, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
-  if (gemm_down_bn(H) == 256)
-    return launch_grouped<256, false>(a_h, b_w2, offsets, E, R, H, I, y, H, status, spin_limit, s);
-  return launch_grouped<128, false>(a_h, b_w2, offsets, E, R, H, I, y, H, status, spin_limit, s);
+  const int bn = gemm_down_bn(H);
+  Maps m;
+  if (!a.encode(&m.a128, 128) || !a.encode(&m.a64, 64) || !b.encode(&m.b_full, bn) ||
+      !b.encode(&m.b_half, bn / 2))
+    return cudaErrorInvalidValue;
+  const int NT = H / bn;
+  if (bn == 256) {
+    if (NT % 2 == 0)
+      return launch_grouped<256, false, 2>(m, offsets, E, R, H, I, y, H, status, spin_limit, s);
+    return launch_grouped<256, false, 1>(m, offsets, E, R, H, I, y, H, status, spin_limit, s);
+  }
+  if (NT % 2 == 0)
+    return launch_grouped<128, false, 2>(m, offsets, E, R, H, I, y, H, status, spin_limit, s);
+  return launch_grouped<128, false, 1>(m, offsets, E, R, H, I, y, H, status, spin_limit, s);
 }
 
 }  // namespace moe

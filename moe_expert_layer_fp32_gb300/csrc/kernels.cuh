@@ -41,13 +41,23 @@ cudaError_t launch_copy_rows(const void* x, const int32_t* row_of_slot, int T, i
 cudaError_t launch_prepack(const void* w_gate, const void* w_up, const void* w_down, int E, int H,
                            int I, void* packed, cudaStream_t s);
 
-// grouped GEMM-1 with the SwiGLU epilogue: h [R, I] bf16
-cudaError_t launch_gemm_gate_up(const CUtensorMap& a_xperm, const CUtensorMap& b_w1,
+// A bf16 row-major operand [rows, cols] of a grouped GEMM.  encode() writes a TMA
+// map of it with boxes of 64 columns x box_rows rows and 128-byte swizzle
+// (defined with the ABI, which owns the driver entry point).
+struct GemmOperand {
+  const void* ptr;
+  uint64_t cols, rows;
+  bool encode(CUtensorMap* map, uint32_t box_rows) const;
+};
+
+// grouped GEMM-1 with the SwiGLU epilogue: a = x_perm [R, H], b = packed W1
+// [E*2I, H] -> h [R, I] bf16
+cudaError_t launch_gemm_gate_up(const GemmOperand& a, const GemmOperand& b,
                                 const int32_t* offsets, int E, int R, int H, int I, void* h,
                                 int32_t* status, long long spin_limit, cudaStream_t s);
 
-// grouped GEMM-2: y [R, H] fp32
-cudaError_t launch_gemm_down(const CUtensorMap& a_h, const CUtensorMap& b_w2,
+// grouped GEMM-2: a = h [R, I], b = packed W2 [E*H, I] -> y [R, H] fp32
+cudaError_t launch_gemm_down(const GemmOperand& a, const GemmOperand& b,
                              const int32_t* offsets, int E, int R, int H, int I, float* y,
                              int32_t* status, long long spin_limit, cudaStream_t s);
 

@@ -129,20 +129,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [outer, inner] row-major, box [box_outer, 64], 128-byte swizzle.
-moe_status make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
-                    uint32_t box_outer) {
+}  // namespace
+
+bool GemmOperand::encode(CUtensorMap* m, uint32_t box_rows) const {
   auto fn = encode_fn();
-  if (fn == nullptr) return MOE_ERR_CUDA;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, box_outer};
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+  return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 // ------------------------------------------------------------ step bodies ---
 moe_status do_load_stats(const int32_t* idx, const moe_dims& d, int32_t* counts,
@@ -175,11 +177,10 @@ moe_status do_expert_ffn(const void* x_perm, const int32_t* offsets, const void*
   void* h = at<void>(ws, L.h);
   const uint16_t* w1 = static_cast<const uint16_t*>(packed);
   const uint16_t* w2 = w1 + (size_t)d.E * 2 * d.I * d.H;
-  CUtensorMap ma, mb, mh, md;
-  MOE_TRY(make_map(&ma, x_perm, d.H, R, 128));
-  MOE_TRY(make_map(&mb, w1, d.H, (uint64_t)d.E * 2 * d.I, 256));
-  MOE_TRY(make_map(&mh, h, d.I, R, 128));
-  MOE_TRY(make_map(&md, w2, d.I, (uint64_t)d.E * d.H, gemm_down_bn(d.H)));
+  const GemmOperand ma{x_perm, (uint64_t)d.H, (uint64_t)R};
+  const GemmOperand mb{w1, (uint64_t)d.H, (uint64_t)d.E * 2 * d.I};
+  const GemmOperand mh{h, (uint64_t)d.I, (uint64_t)R};
+  const GemmOperand md{w2, (uint64_t)d.I, (uint64_t)d.E * d.H};
   MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, d.E, R, d.H, d.I, h, status, kSpinLimitCycles, s));
   if (after_gate_up != nullptr) MOE_CUDA(cudaEventRecord(after_gate_up, s));
   MOE_CUDA(launch_gemm_down(mh, md, offsets, d.E, R, d.H, d.I, y, status, kSpinLimitCycles, s));
