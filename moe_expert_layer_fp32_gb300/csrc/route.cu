@@ -6,14 +6,18 @@
 // probabilities are selected and renormalised by adding them left to right and
 // dividing each by the sum; experts are returned sorted by probability.
 //
-// Kernel shape.  One CTA = 64 tokens x all E experts (E padded to EP in
-// {32, 64, 128, 256}); 256 threads = 8 warps.  Warp w owns tokens 8w..8w+7; lane
-// i owns EP/32 experts (4i + 128g + jj for EP >= 128, else EP/32 consecutive).
-// Each logit is ONE thread's fused multiply-add chain over h = 0, 1, ..., H-1
-// starting from 0 (no split of K, no tree), then one FP32 add of the bias: the
-// same bits as the CPU reference FMA chain, and independent of T.  x is widened
-// to FP32 once per 32-column chunk into shared memory (transposed, so a warp's
-// token reads are broadcasts); W_r chunks are staged beside it.
+// Kernel shape.  One CTA = 32 tokens x all E experts (E padded to EP in
+// {32, 64, 128, 256}); 128 threads = 4 warps, four CTAs per SM.  Warp w owns
+// tokens 8w..8w+7; lane i owns EP/32 experts (4i + 128g + jj for EP >= 128, else
+// EP/32 consecutive).  Each logit is ONE thread's fused multiply-add chain over
+// h = 0, 1, ..., H-1 starting from 0 (no split of K, no tree), then one FP32 add
+// of the bias: the same bits as a CPU FMA chain, and independent of T.
+//
+// Data movement: 16-column chunks of W_r (FP32) and x (bf16) are copied into a
+// double-buffered shared-memory ring with cp.async while the previous chunk is
+// multiplied; x is then widened once to FP32 into a transposed buffer, so a
+// warp's eight token values for one h are two broadcast loads.  Small CTAs (32
+// tokens) keep each SM's share of T within a few percent of the mean.
 //
 // Epilogue: logits go to shared memory; one warp per token runs k rounds of a
 // warp-wide argmax under the key (logit desc, expert asc), then the softmax
@@ -28,16 +32,19 @@
 namespace moe {
 namespace {
 
-constexpr int BT = 64;       // tokens per CTA
-constexpr int HK = 32;       // hidden columns per chunk
-constexpr int XLD = BT + 4;  // row stride of the transposed x chunk (16-byte aligned rows)
+constexpr int BT = 32;       // tokens per CTA
+constexpr int HK = 16;       // hidden columns per chunk
+constexpr int XLD = BT + 4;  // row stride of the transposed FP32 x chunk
+constexpr int NTHR = 128;
 
 template <int EP>
 struct RouteSmem {
-  static constexpr int chunk_floats = HK * XLD + HK * EP;
-  static constexpr int logit_floats = BT * (EP + 1);
-  static constexpr int bytes =
-      4 * (chunk_floats > logit_floats ? chunk_floats : logit_floats);
+  static constexpr int w_floats = 2 * HK * EP;         // W_r ring
+  static constexpr int xst_halves = 2 * BT * HK;       // bf16 x ring
+  static constexpr int xs_floats = HK * XLD;           // FP32 transposed x
+  static constexpr int ring_bytes = 4 * w_floats + 2 * xst_halves + 4 * xs_floats;
+  static constexpr int logit_bytes = 4 * BT * (EP + 1);
+  static constexpr int bytes = ring_bytes > logit_bytes ? ring_bytes : logit_bytes;
 };
 
 template <int EP>
@@ -51,21 +58,59 @@ __device__ __forceinline__ int expert_of(int lane, int jj) {
 }
 
 template <int EP>
-__global__ void __launch_bounds__(256) route_kernel(const uint16_t* __restrict__ x,
-                                                    const float* __restrict__ wr,
-                                                    const float* __restrict__ bias, int T, int H,
-                                                    int E, int k, int32_t* __restrict__ topk_idx,
-                                                    float* __restrict__ topk_w) {
-  constexpr int TE = EP / 32;   // experts per thread
-  constexpr int TT = 8;         // tokens per thread
-  constexpr int WPT = EP / 8;   // W_r chunk elements loaded per thread (HK*EP/256)
+__global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restrict__ x,
+                                                        const float* __restrict__ wr,
+                                                        const float* __restrict__ bias, int T,
+                                                        int H, int E, int k,
+                                                        int32_t* __restrict__ topk_idx,
+                                                        float* __restrict__ topk_w) {
+  constexpr int TE = EP / 32;  // experts per thread
+  constexpr int TT = 8;        // tokens per thread (one warp = 8 tokens)
   extern __shared__ float4 smem_f4[];
-  float* smem = reinterpret_cast<float*>(smem_f4);
-  float* xs = smem;             // [HK][XLD]   x chunk, transposed, FP32
-  float* ws = smem + HK * XLD;  // [HK][EP]    W_r chunk, zero beyond E
+  float* ws = reinterpret_cast<float*>(smem_f4);                      // [2][HK][EP]
+  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + 2 * HK * EP);      // [2][BT][HK]
+  float* xs = reinterpret_cast<float*>(xst + 2 * BT * HK);            // [HK][XLD]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * BT;
+  const int nchunks = H / HK;
+  const bool vec_w = (E % 4) == 0;
+
+  // Padding experts (E..EP-1) read zeros from both ring buffers for the whole kernel.
+  if (E < EP) {
+    for (int i = tid; i < 2 * HK * EP; i += NTHR)
+      if ((i % EP) >= E) ws[i] = 0.0f;
+  }
+
+  auto issue_chunk = [&](int c, int buf) {
+    const int h0 = c * HK;
+    float* wdst = ws + buf * HK * EP;
+    if (E == EP) {
+      // W_r rows h0..h0+HK-1 are contiguous and unpadded: a flat 16-byte copy
+      const float* src = wr + (size_t)h0 * E;
+#pragma unroll
+      for (int i = tid; i < HK * EP / 4; i += NTHR) cp_async_16(wdst + 4 * i, src + 4 * i, 16);
+    } else if (vec_w) {
+      const int n4 = HK * E / 4;  // 16-byte pieces
+      const float* src = wr + (size_t)h0 * E;
+      for (int i = tid; i < n4; i += NTHR) {
+        const int f = 4 * i;
+        cp_async_16(wdst + (f / E) * EP + (f % E), src + f, 16);
+      }
+    } else {
+      const float* src = wr + (size_t)h0 * E;
+      for (int i = tid; i < HK * E; i += NTHR) cp_async_4(wdst + (i / E) * EP + (i % E), src + i);
+    }
+    // x chunk: BT rows x HK bf16 = two 16-byte pieces per row; rows past T are zero
+    uint16_t* xdst = xst + buf * BT * HK;
+    if (tid < 2 * BT) {
+      const int r = tid >> 1, half = tid & 1;
+      const int t = t0 + r;
+      const uint16_t* src = (t < T) ? x + (size_t)t * H + h0 + 8 * half : x;
+      cp_async_16(xdst + r * HK + 8 * half, src, (t < T) ? 16 : 0);
+    }
+    cp_async_commit();
+  };
 
   float acc[TT][TE];
 #pragma unroll
@@ -73,42 +118,28 @@ __global__ void __launch_bounds__(256) route_kernel(const uint16_t* __restrict__
 #pragma unroll
     for (int j = 0; j < TE; ++j) acc[i][j] = 0.0f;
 
-  // global -> register staging of one chunk
-  const int xr = tid >> 2, xc = (tid & 3) * 8;  // 64 rows x 4 pieces of 8 bf16
-  const int xt = t0 + xr;
-  uint4 xreg;
-  float wreg[WPT];
-  auto load_chunk = [&](int h0) {
-    xreg = make_uint4(0, 0, 0, 0);
-    if (xt < T) xreg = __ldg(reinterpret_cast<const uint4*>(x + (size_t)xt * H + h0 + xc));
-#pragma unroll
-    for (int i = 0; i < WPT; ++i) {
-      int f = tid + i * 256;
-      int r = f / EP, c = f % EP;
-      wreg[i] = (c < E) ? __ldg(wr + (size_t)(h0 + r) * E + c) : 0.0f;
+  issue_chunk(0, 0);
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = c & 1;
+    if (c + 1 < nchunks) {
+      issue_chunk(c + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
-  };
-  auto store_chunk = [&]() {
-    const uint32_t xw[4] = {xreg.x, xreg.y, xreg.z, xreg.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      xs[(xc + 2 * q) * XLD + xr] = bf16_lo(xw[q]);
-      xs[(xc + 2 * q + 1) * XLD + xr] = bf16_hi(xw[q]);
-    }
-#pragma unroll
-    for (int i = 0; i < WPT; ++i) {
-      int f = tid + i * 256;
-      ws[(f / EP) * EP + (f % EP)] = wreg[i];
-    }
-  };
-
-  load_chunk(0);
-  for (int h0 = 0; h0 < H; h0 += HK) {
     __syncthreads();
-    store_chunk();
+    // widen the x chunk to FP32, transposed: xs[h][token]
+    {
+      const int r = tid >> 2, hq = (tid & 3) * 4;  // 32 rows x 4 groups of 4 columns
+      const uint2 v = *reinterpret_cast<const uint2*>(xst + buf * BT * HK + r * HK + hq);
+      xs[(hq + 0) * XLD + r] = bf16_lo(v.x);
+      xs[(hq + 1) * XLD + r] = bf16_hi(v.x);
+      xs[(hq + 2) * XLD + r] = bf16_lo(v.y);
+      xs[(hq + 3) * XLD + r] = bf16_hi(v.y);
+    }
     __syncthreads();
-    if (h0 + HK < H) load_chunk(h0 + HK);
-#pragma unroll 4
+    const float* wsb = ws + buf * HK * EP;
+#pragma unroll
     for (int hh = 0; hh < HK; ++hh) {
       const float4 xa = *reinterpret_cast<const float4*>(xs + hh * XLD + warp * TT);
       const float4 xb = *reinterpret_cast<const float4*>(xs + hh * XLD + warp * TT + 4);
@@ -117,30 +148,30 @@ __global__ void __launch_bounds__(256) route_kernel(const uint16_t* __restrict__
       if constexpr (TE >= 4) {
 #pragma unroll
         for (int g = 0; g < TE / 4; ++g) {
-          const float4 w4 = *reinterpret_cast<const float4*>(ws + hh * EP + g * 128 + lane * 4);
+          const float4 w4 = *reinterpret_cast<const float4*>(wsb + hh * EP + g * 128 + lane * 4);
           wv[4 * g + 0] = w4.x;
           wv[4 * g + 1] = w4.y;
           wv[4 * g + 2] = w4.z;
           wv[4 * g + 3] = w4.w;
         }
       } else if constexpr (TE == 2) {
-        const float2 w2 = *reinterpret_cast<const float2*>(ws + hh * EP + lane * 2);
+        const float2 w2 = *reinterpret_cast<const float2*>(wsb + hh * EP + lane * 2);
         wv[0] = w2.x;
         wv[1] = w2.y;
       } else {
-        wv[0] = ws[hh * EP + lane];
+        wv[0] = wsb[hh * EP + lane];
       }
 #pragma unroll
       for (int i = 0; i < TT; ++i)
 #pragma unroll
         for (int j = 0; j < TE; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
     }
+    __syncthreads();
   }
 
   // ---- epilogue: logits (+ bias) to shared memory --------------------------
-  __syncthreads();
   constexpr int LLD = EP + 1;
-  float* ls = smem;  // [BT][LLD]
+  float* ls = reinterpret_cast<float*>(smem_f4);  // [BT][LLD], over the drained ring
 #pragma unroll
   for (int j = 0; j < TE; ++j) {
     const int e = expert_of<EP>(lane, j);
@@ -239,8 +270,8 @@ cudaError_t launch_ep(const void* x, const float* wr, const float* bias, int T, 
     attr_set[dev] = true;
   }
   dim3 grid((T + BT - 1) / BT);
-  route_kernel<EP><<<grid, 256, smem, s>>>(static_cast<const uint16_t*>(x), wr, bias, T, H, E, k,
-                                           idx, w);
+  route_kernel<EP><<<grid, NTHR, smem, s>>>(static_cast<const uint16_t*>(x), wr, bias, T, H, E,
+                                            k, idx, w);
   return cudaGetLastError();
 }
 
