@@ -227,3 +227,51 @@ def layer_forward(x, w_router, bias, packed, d, workspace, stream=None, want_rou
         counts = torch.empty(d.E, dtype=torch.int32, device=dev)
     moe_layer_fwd(x, w_router, bias, packed, d, out, idx, w, counts, workspace, stream)
     return (out, idx, w, counts) if want_routing else out
+
+
+def layer_forward_host_batches(x_host_batches, w_router, bias, packed, d, out_host_batches,
+                               workspace, stream=None):
+    """Forward a sequence of token batches that live in pinned host memory, writing each
+    batch's output back to pinned host memory.
+
+    Transfers overlap compute: batch i+1 is copied to the device on one copy stream
+    while batch i runs (moe_layer_fwd on `stream`, default the current stream), and
+    batch i's output is copied back on a second copy stream while batch i+1 runs.
+    Two device buffers per direction rotate.  Every batch must have d.T tokens.
+    Returns once all work is enqueued; synchronise `stream` (or the last event) to
+    read the outputs.
+    """
+    compute = torch.cuda.current_stream() if stream is None else stream
+    dev = torch.device("cuda", torch.cuda.current_device())
+    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    h2d.wait_stream(compute)  # nothing starts before work already queued on the caller's stream
+    x_dev = [torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    o_dev = [torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    copied_in = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    copied_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+    for i, (xh, oh) in enumerate(zip(x_host_batches, out_host_batches)):
+        b = i & 1
+        if used[b]:
+            h2d.wait_event(computed[b])        # batch i-2 no longer reads x_dev[b]
+        with torch.cuda.stream(h2d):
+            x_dev[b].copy_(xh, non_blocking=True)
+            copied_in[b].record(h2d)
+        compute.wait_event(copied_in[b])
+        if used[b]:
+            compute.wait_event(copied_out[b])  # batch i-2's output has left o_dev[b]
+        moe_layer_fwd(x_dev[b], w_router, bias, packed, d, o_dev[b], None, None, None, workspace,
+                      compute)
+        computed[b].record(compute)
+        d2h.wait_event(computed[b])
+        with torch.cuda.stream(d2h):
+            oh.copy_(o_dev[b], non_blocking=True)
+            copied_out[b].record(d2h)
+        used[b] = True
+    for e in copied_out:
+        compute.wait_event(e)                  # the caller's stream covers the last copies
+    for t in x_dev + o_dev:
+        t.record_stream(h2d)
+        t.record_stream(d2h)
+    return compute

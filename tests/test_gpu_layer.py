@@ -97,3 +97,23 @@ def test_run_twice_identical_bytes(moe):
     b = run_layer(moe, wl, W, x, wr, bias)
     for u, v in zip(a, b):
         np.testing.assert_array_equal(u.view(np.uint8), v.view(np.uint8))
+
+
+def test_host_batches_pipeline_matches_device_calls(moe):
+    """layer_forward_host_batches (pinned host in/out, transfers overlapped with
+    compute) gives the same bytes as one moe_layer_fwd per batch."""
+    wl = synth.WORKLOADS["fine_grained"]
+    W = weights(wl)
+    T = 512
+    xs = [synth.tokens(wl, rows=np.arange(i * T, (i + 1) * T)) for i in range(5)]
+    wr, bias = synth.router(wl)
+    d = moe.dims(T, wl.H, wl.E, wl.k, wl.I)
+    ws = moe.new_workspace(d)
+    x_pin = [torch.from_numpy(x.view(np.int16)).pin_memory().view(torch.bfloat16) for x in xs]
+    o_pin = [torch.zeros((T, wl.H), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    moe.layer_forward_host_batches(x_pin, dev(wr), dev(bias), W.packed, d, o_pin, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    for x, o in zip(xs, o_pin):
+        ref, _, _, _ = run_layer(moe, wl, W, x, wr, bias)
+        np.testing.assert_array_equal(o.view(torch.int16).numpy().view(np.uint16), ref)
