@@ -117,3 +117,35 @@ def test_host_batches_pipeline_matches_device_calls(moe):
     for x, o in zip(xs, o_pin):
         ref, _, _, _ = run_layer(moe, wl, W, x, wr, bias)
         np.testing.assert_array_equal(o.view(torch.int16).numpy().view(np.uint16), ref)
+
+
+@pytest.mark.parametrize("name", ["fine_grained", "packed_rl", "tiny"])
+def test_layer_equals_step_by_step_calls(moe, name):
+    """moe_layer_fwd (combine fused into the down GEMM) gives the same bytes as the
+    step-by-step ABI calls ending in the stand-alone moe_combine."""
+    wl = synth.WORKLOADS[name]
+    W = weights(wl)
+    x = synth.tokens(wl)
+    wr, bias = synth.router(wl)
+    out_layer, idx_l, w_l, _ = run_layer(moe, wl, W, x, wr, bias)
+    T, R = wl.T, wl.T * wl.k
+    d = moe.dims(T, wl.H, wl.E, wl.k, wl.I)
+    ws = moe.new_workspace(d)
+    xd = dev_bf16(x)
+    idx = torch.empty((T, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, wl.k), dtype=torch.float32, device="cuda")
+    moe.moe_route(xd, dev(wr), None if bias is None else dev(bias), d, idx, w)
+    counts = torch.empty(wl.E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(wl.E + 1, dtype=torch.int32, device="cuda")
+    moe.moe_load_stats(idx, d, counts, offsets, ws)
+    xp = torch.empty((R, wl.H), dtype=torch.bfloat16, device="cuda")
+    ros = torch.empty(R, dtype=torch.int32, device="cuda")
+    sor = torch.empty(R, dtype=torch.int32, device="cuda")
+    moe.moe_permute(xd, idx, offsets, d, xp, ros, sor, ws)
+    y = torch.empty((R, wl.H), dtype=torch.float32, device="cuda")
+    moe.moe_expert_ffn(xp, offsets, W.packed, d, y, ws)
+    out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_combine(y, w, ros, d, out)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    np.testing.assert_array_equal(bits(out), out_layer)
