@@ -155,6 +155,61 @@ __global__ void __launch_bounds__(PB) rank_kernel(const int32_t* __restrict__ to
   }
 }
 
+// T <= 256 (a single ranking block): masks, counts, offsets and stable ranks in
+// one CTA, the work of block_counts + scan + rank without two launches.
+__global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __restrict__ topk_idx,
+                                                            int T, int k, int E,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ row_of_slot,
+                                                            int32_t* __restrict__ slot_of_row,
+                                                            int32_t* status) {
+  extern __shared__ uint32_t smem_u[];
+  uint32_t* masks = smem_u;
+  int32_t* sidx = reinterpret_cast<int32_t*>(smem_u + 8 * E);
+  __shared__ int s_scan[kMaxE];
+  build_masks(topk_idx, T, k, E, 0, masks, sidx, status);
+  const int tid = threadIdx.x;
+  int c = 0;
+  if (tid < E) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) c += __popc(masks[w * E + tid]);
+  }
+  s_scan[tid] = c;  // blockDim == kMaxE
+  __syncthreads();
+  for (int off = 1; off < kMaxE; off <<= 1) {
+    const int v = (tid >= off) ? s_scan[tid - off] : 0;
+    __syncthreads();
+    s_scan[tid] += v;
+    __syncthreads();
+  }
+  const int excl = s_scan[tid] - c;
+  if (tid < E) {
+    counts[tid] = c;
+    offsets[tid] = excl;
+  }
+  if (tid == 0) offsets[E] = s_scan[kMaxE - 1];
+  __syncthreads();
+  s_scan[tid] = excl;  // first row of each expert
+  __syncthreads();
+  const int lane = tid & 31, warp = tid >> 5;
+  if (tid >= T) return;
+  const uint32_t below = (1u << lane) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const int e = sidx[tid * k + j];
+    const size_t s = (size_t)tid * k + j;
+    if (e < 0 || e >= E) {
+      row_of_slot[s] = -1;
+      continue;
+    }
+    int rank = __popc(masks[warp * E + e] & below);
+    for (int w = 0; w < warp; ++w) rank += __popc(masks[w * E + e]);
+    const int row = s_scan[e] + rank;
+    row_of_slot[s] = row;
+    slot_of_row[row] = (int32_t)s;
+  }
+}
+
 // One warp per token: read the row once (16-byte vectors), write it to its k rows.
 __global__ void __launch_bounds__(256) copy_rows_kernel(const uint16_t* __restrict__ x,
                                                         const int32_t* __restrict__ row_of_slot,
@@ -221,6 +276,14 @@ cudaError_t launch_rank(const int32_t* topk_idx, int T, int k, int E, const int3
   const int nb = (T + PB - 1) / PB;
   rank_kernel<<<nb, PB, mask_smem_bytes(E, k), s>>>(topk_idx, T, k, E, blk_base, row_of_slot,
                                                     slot_of_row, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, int32_t* counts,
+                                  int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,
+                                  int32_t* status, cudaStream_t s) {
+  dispatch_small_kernel<<<1, PB, mask_smem_bytes(E, k), s>>>(topk_idx, T, k, E, counts, offsets,
+                                                             row_of_slot, slot_of_row, status);
   return cudaGetLastError();
 }
 

@@ -188,20 +188,22 @@ __global__ void __launch_bounds__(192, 1)
   const int rank = (CL == 2) ? (int)cluster_ctarank() : 0;
   const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
 
+  // all threads bring the offsets in at once; thread 0 then builds the schedule from
+  // shared memory (a serial walk over global memory would cost E load latencies)
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = __ldg(offsets + e);
+  __syncthreads();
   if (threadIdx.x == 0) {
     // schedule: validate offsets (0 = o_0 <= o_1 <= ... <= o_E = R), work prefix
-    bool ok = __ldg(offsets) == 0 && __ldg(offsets + E) == R;
+    bool ok = s_off[0] == 0 && s_off[E] == R;
     int p = 0;
     for (int e = 0; e < E; ++e) {
-      const int a = __ldg(offsets + e), b = __ldg(offsets + e + 1);
+      const int a = s_off[e], b = s_off[e + 1];
       if (b < a) ok = false;
       const int mt = b > a ? (b - a + GM - 1) / GM : 0;
-      s_off[e] = a;
       s_mt[e] = mt;
       s_prefix[e] = p;
       p += mt * NT / CL;  // CL == 2 only when NT is even
     }
-    s_off[E] = __ldg(offsets + E);
     if (!ok) {
       flag_error(status, MOE_ERR_DEVICE_CHECK);
       for (int e = 0; e < E; ++e) s_prefix[e] = 0;

@@ -12,6 +12,7 @@ constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
 constexpr int kPermBlock = 256;  // tokens per ranking block of the permutation
 constexpr long long kSpinLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr int kRouteSmallMaxT = 64;  // batches up to this size use the small-T router kernel
 
 // router: projection (FP32 FMA chain), softmax, top-k, renormalisation
 cudaError_t launch_route(const void* x, const float* w_router, const float* bias, int T, int H,
@@ -31,6 +32,11 @@ cudaError_t launch_scan(const int32_t* blk_counts, int nb, int E, int R, int32_t
 cudaError_t launch_rank(const int32_t* topk_idx, int T, int k, int E, const int32_t* blk_base,
                         int32_t* row_of_slot, int32_t* slot_of_row, int32_t* status,
                         cudaStream_t s);
+
+// T <= kPermBlock: counts, offsets, row_of_slot and slot_of_row in one launch
+cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, int32_t* counts,
+                                  int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,
+                                  int32_t* status, cudaStream_t s);
 
 // x_perm[row_of_slot[t*k+j]] = x[t]
 cudaError_t launch_copy_rows(const void* x, const int32_t* row_of_slot, int T, int H, int k,

@@ -220,9 +220,17 @@ moe_status layer_fwd(const void* x, const float* w_router, const float* bias,
   MOE_TRY(mark(0));
   MOE_CUDA(launch_route(x, w_router, bias, d.T, d.H, d.E, d.k, idx, w, s));
   MOE_TRY(mark(1));
-  MOE_TRY(do_load_stats(idx, d, counts, offsets, false, workspace, s));
-  MOE_TRY(mark(2));
-  if (d.T > 0) MOE_TRY(do_permute_rows(x, idx, d, x_perm, ros, sor, workspace, s));
+  if (d.T > 0 && d.T <= kPermBlock) {
+    // one ranking block: counts, offsets and ranks in a single launch
+    MOE_CUDA(launch_dispatch_small(idx, d.T, d.k, d.E, counts, offsets, ros, sor,
+                                   at<int32_t>(workspace, L.status), s));
+    MOE_TRY(mark(2));
+    MOE_CUDA(launch_copy_rows(x, ros, d.T, d.H, d.k, x_perm, at<int32_t>(workspace, L.status), s));
+  } else {
+    MOE_TRY(do_load_stats(idx, d, counts, offsets, false, workspace, s));
+    MOE_TRY(mark(2));
+    if (d.T > 0) MOE_TRY(do_permute_rows(x, idx, d, x_perm, ros, sor, workspace, s));
+  }
   MOE_TRY(mark(3));
   if (d.T > 0)
     MOE_TRY(do_expert_ffn(x_perm, offsets, packed_weights, d, y, workspace, s,

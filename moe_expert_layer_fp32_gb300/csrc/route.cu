@@ -6,22 +6,27 @@
 // probabilities are selected and renormalised by adding them left to right and
 // dividing each by the sum; experts are returned sorted by probability.
 //
-// Kernel shape.  One CTA = 32 tokens x all E experts (E padded to EP in
-// {32, 64, 128, 256}); 128 threads = 4 warps, four CTAs per SM.  Warp w owns
-// tokens 8w..8w+7; lane i owns EP/32 experts (4i + 128g + jj for EP >= 128, else
-// EP/32 consecutive).  Each logit is ONE thread's fused multiply-add chain over
+// In both kernels below each logit is ONE thread's fused multiply-add chain over
 // h = 0, 1, ..., H-1 starting from 0 (no split of K, no tree), then one FP32 add
-// of the bias: the same bits as a CPU FMA chain, and independent of T.
+// of the bias, and both finish with the same per-token epilogue: the routing of
+// a token is the same bits whichever kernel runs and whatever T is.
 //
-// Data movement: 16-column chunks of W_r (FP32) and x (bf16) are copied into a
-// double-buffered shared-memory ring with cp.async while the previous chunk is
-// multiplied; x is then widened once to FP32 into a transposed buffer, so a
-// warp's eight token values for one h are two broadcast loads.  Small CTAs (32
-// tokens) keep each SM's share of T within a few percent of the mean.
+// route_kernel (T large): one CTA = 32 tokens x all E experts (E padded to EP
+// in {32, 64, 128, 256}); 128 threads = 4 warps, up to four CTAs per SM.  Warp w
+// owns tokens 8w..8w+7; lane i owns EP/32 experts (4i + 128g + jj for EP >= 128,
+// else EP/32 consecutive).  Chunks of HK = 4096/EP hidden columns (16 KB of W_r)
+// and the matching x columns are copied by cp.async into a 3-stage ring while
+// earlier chunks are multiplied (four CTAs fit on an SM); x is widened once to FP32 into a transposed
+// buffer, so a warp's eight token values for one h are two broadcast loads.
 //
-// Epilogue: logits go to shared memory; one warp per token runs k rounds of a
-// warp-wide argmax under the key (logit desc, expert asc), then the softmax
-// denominator (lane partial sums in ascending expert order, then an xor
+// route_small_kernel (T small): one CTA = 1, 2, 4 or 8 tokens; thread (g, e) owns
+// expert e for a group of the CTA's tokens; W_r and x stream through a six-stage
+// cp.async ring of 16 KB W_r chunks (about 100 KB in flight), since with few
+// CTAs the K loop is bound by how much of W_r each one keeps in flight.
+//
+// Epilogue (shared): logits go to shared memory; one warp per token runs k
+// rounds of a warp-wide argmax under the key (logit desc, expert asc), then the
+// softmax denominator (lane partial sums in ascending expert order, then an xor
 // butterfly: identical bits on every lane and for every T).  Selection uses the
 // FP32 logit, which orders experts exactly as the probabilities do.
 #include <math.h>
@@ -32,16 +37,17 @@
 namespace moe {
 namespace {
 
-constexpr int BT = 32;       // tokens per CTA
-constexpr int HK = 16;       // hidden columns per chunk
+constexpr int BT = 32;       // tokens per CTA (large-T kernel)
 constexpr int XLD = BT + 4;  // row stride of the transposed FP32 x chunk
 constexpr int NTHR = 128;
+constexpr int NST = 3;       // cp.async ring depth
 
 template <int EP>
-struct RouteSmem {
-  static constexpr int w_floats = 2 * HK * EP;         // W_r ring
-  static constexpr int xst_halves = 2 * BT * HK;       // bf16 x ring
-  static constexpr int xs_floats = HK * XLD;           // FP32 transposed x
+struct RouteCfg {
+  static constexpr int HK = (2048 / EP > 16) ? 2048 / EP : 16;  // 8-16 KB of W_r per chunk
+  static constexpr int w_floats = NST * HK * EP;        // W_r ring
+  static constexpr int xst_halves = NST * BT * HK;      // bf16 x ring
+  static constexpr int xs_floats = HK * XLD;            // FP32 transposed x
   static constexpr int ring_bytes = 4 * w_floats + 2 * xst_halves + 4 * xs_floats;
   static constexpr int logit_bytes = 4 * BT * (EP + 1);
   static constexpr int bytes = ring_bytes > logit_bytes ? ring_bytes : logit_bytes;
@@ -57,6 +63,77 @@ __device__ __forceinline__ int expert_of(int lane, int jj) {
   }
 }
 
+// One warp routes token t from its E logits lrow[0..E) (shared memory): top-k by
+// (logit desc, expert asc), FP32 softmax over all E, renormalised weights.
+template <int EP>
+__device__ __forceinline__ void route_one_token(const float* lrow, int E, int k, int lane, int t,
+                                                int32_t* __restrict__ topk_idx,
+                                                float* __restrict__ topk_w) {
+  constexpr int NV = EP / 32;
+  float v[NV];
+  unsigned taken = 0;
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    const int e = lane + 32 * q;
+    v[q] = (e < E) ? lrow[e] : -INFINITY;
+    if (e >= E) taken |= 1u << q;
+  }
+  float sel_l[kMaxK];
+  int sel_e[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j < k) {
+      float bv = -INFINITY;
+      int be = 0x7FFFFFFF;
+#pragma unroll
+      for (int q = 0; q < NV; ++q) {
+        const int e = lane + 32 * q;
+        if (!((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
+          bv = v[q];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+        const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      sel_l[j] = bv;
+      sel_e[j] = be;
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    }
+  }
+  // softmax denominator over all E experts, max-shifted
+  const float m = sel_l[0];
+  float z = 0.0f;
+#pragma unroll
+  for (int q = 0; q < NV; ++q)
+    if (lane + 32 * q < E) z = __fadd_rn(z, expf(v[q] - m));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z = __fadd_rn(z, __shfl_xor_sync(0xFFFFFFFFu, z, off));
+  // selected probabilities, their left-to-right sum, renormalised weights
+  float p[kMaxK];
+  float S = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j < k) {
+      p[j] = __fdiv_rn(expf(sel_l[j] - m), z);
+      S = __fadd_rn(S, p[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j < k && lane == j) {
+      topk_idx[(size_t)t * k + j] = sel_e[j];
+      topk_w[(size_t)t * k + j] = __fdiv_rn(p[j], S);
+    }
+  }
+}
+
 template <int EP>
 __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restrict__ x,
                                                         const float* __restrict__ wr,
@@ -64,52 +141,56 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
                                                         int H, int E, int k,
                                                         int32_t* __restrict__ topk_idx,
                                                         float* __restrict__ topk_w) {
+  using C = RouteCfg<EP>;
+  constexpr int HK = C::HK;
   constexpr int TE = EP / 32;  // experts per thread
   constexpr int TT = 8;        // tokens per thread (one warp = 8 tokens)
   extern __shared__ float4 smem_f4[];
-  float* ws = reinterpret_cast<float*>(smem_f4);                      // [2][HK][EP]
-  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + 2 * HK * EP);      // [2][BT][HK]
-  float* xs = reinterpret_cast<float*>(xst + 2 * BT * HK);            // [HK][XLD]
+  float* ws = reinterpret_cast<float*>(smem_f4);                      // [NST][HK][EP]
+  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + NST * HK * EP);    // [NST][BT][HK]
+  float* xs = reinterpret_cast<float*>(xst + NST * BT * HK);          // [HK][XLD]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * BT;
   const int nchunks = H / HK;
   const bool vec_w = (E % 4) == 0;
 
-  // Padding experts (E..EP-1) read zeros from both ring buffers for the whole kernel.
+  // Padding experts (E..EP-1) read zeros from every ring buffer for the whole kernel.
   if (E < EP) {
-    for (int i = tid; i < 2 * HK * EP; i += NTHR)
+    for (int i = tid; i < NST * HK * EP; i += NTHR)
       if ((i % EP) >= E) ws[i] = 0.0f;
   }
 
-  auto issue_chunk = [&](int c, int buf) {
-    const int h0 = c * HK;
-    float* wdst = ws + buf * HK * EP;
-    if (E == EP) {
-      // W_r rows h0..h0+HK-1 are contiguous and unpadded: a flat 16-byte copy
-      const float* src = wr + (size_t)h0 * E;
+  auto issue_chunk = [&](int c) {
+    if (c < nchunks) {
+      const int buf = c % NST;
+      const int h0 = c * HK;
+      float* wdst = ws + buf * HK * EP;
+      const float* wsrc = wr + (size_t)h0 * E;
+      if (E == EP) {
+        // W_r rows h0..h0+HK-1 are contiguous and unpadded: a flat 16-byte copy
 #pragma unroll
-      for (int i = tid; i < HK * EP / 4; i += NTHR) cp_async_16(wdst + 4 * i, src + 4 * i, 16);
-    } else if (vec_w) {
-      const int n4 = HK * E / 4;  // 16-byte pieces
-      const float* src = wr + (size_t)h0 * E;
-      for (int i = tid; i < n4; i += NTHR) {
-        const int f = 4 * i;
-        cp_async_16(wdst + (f / E) * EP + (f % E), src + f, 16);
+        for (int i = tid; i < HK * EP / 4; i += NTHR) cp_async_16(wdst + 4 * i, wsrc + 4 * i, 16);
+      } else if (vec_w) {
+        for (int i = tid; i < HK * E / 4; i += NTHR) {
+          const int f = 4 * i;
+          cp_async_16(wdst + (f / E) * EP + (f % E), wsrc + f, 16);
+        }
+      } else {
+        for (int i = tid; i < HK * E; i += NTHR)
+          cp_async_4(wdst + (i / E) * EP + (i % E), wsrc + i);
       }
-    } else {
-      const float* src = wr + (size_t)h0 * E;
-      for (int i = tid; i < HK * E; i += NTHR) cp_async_4(wdst + (i / E) * EP + (i % E), src + i);
+      // x chunk: BT rows x HK bf16 in 16-byte pieces; rows past T are zero
+      uint16_t* xdst = xst + buf * BT * HK;
+      constexpr int PPR = HK / 8;  // pieces per row
+      for (int i = tid; i < BT * PPR; i += NTHR) {
+        const int r = i / PPR, pc = i % PPR;
+        const int t = t0 + r;
+        const uint16_t* src = (t < T) ? x + (size_t)t * H + h0 + 8 * pc : x;
+        cp_async_16(xdst + r * HK + 8 * pc, src, (t < T) ? 16 : 0);
+      }
     }
-    // x chunk: BT rows x HK bf16 = two 16-byte pieces per row; rows past T are zero
-    uint16_t* xdst = xst + buf * BT * HK;
-    if (tid < 2 * BT) {
-      const int r = tid >> 1, half = tid & 1;
-      const int t = t0 + r;
-      const uint16_t* src = (t < T) ? x + (size_t)t * H + h0 + 8 * half : x;
-      cp_async_16(xdst + r * HK + 8 * half, src, (t < T) ? 16 : 0);
-    }
-    cp_async_commit();
+    cp_async_commit();  // one group per chunk slot, empty past the end
   };
 
   float acc[TT][TE];
@@ -118,19 +199,16 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
 #pragma unroll
     for (int j = 0; j < TE; ++j) acc[i][j] = 0.0f;
 
-  issue_chunk(0, 0);
+#pragma unroll
+  for (int c = 0; c < NST - 1; ++c) issue_chunk(c);
   for (int c = 0; c < nchunks; ++c) {
-    const int buf = c & 1;
-    if (c + 1 < nchunks) {
-      issue_chunk(c + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    const int buf = c % NST;
+    issue_chunk(c + NST - 1);
+    cp_async_wait<NST - 1>();
     __syncthreads();
     // widen the x chunk to FP32, transposed: xs[h][token]
-    {
-      const int r = tid >> 2, hq = (tid & 3) * 4;  // 32 rows x 4 groups of 4 columns
+    for (int i = tid; i < BT * HK / 4; i += NTHR) {
+      const int r = i / (HK / 4), hq = (i % (HK / 4)) * 4;
       const uint2 v = *reinterpret_cast<const uint2*>(xst + buf * BT * HK + r * HK + hq);
       xs[(hq + 0) * XLD + r] = bf16_lo(v.x);
       xs[(hq + 1) * XLD + r] = bf16_hi(v.x);
@@ -139,7 +217,7 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
     }
     __syncthreads();
     const float* wsb = ws + buf * HK * EP;
-#pragma unroll
+#pragma unroll 8
     for (int hh = 0; hh < HK; ++hh) {
       const float4 xa = *reinterpret_cast<const float4*>(xs + hh * XLD + warp * TT);
       const float4 xb = *reinterpret_cast<const float4*>(xs + hh * XLD + warp * TT + 4);
@@ -168,6 +246,7 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
     }
     __syncthreads();
   }
+  cp_async_wait<0>();
 
   // ---- epilogue: logits (+ bias) to shared memory --------------------------
   constexpr int LLD = EP + 1;
@@ -184,82 +263,159 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
     }
   }
   __syncthreads();
-
-  // ---- softmax / top-k / renormalise: warp w handles its 8 tokens ----------
-  constexpr int NV = EP / 32;
   for (int i = 0; i < TT; ++i) {
     const int tl = warp * TT + i;
     const int t = t0 + tl;
     if (t >= T) break;
-    float v[NV];
-    unsigned taken = 0;
-#pragma unroll
-    for (int q = 0; q < NV; ++q) {
-      const int e = lane + 32 * q;
-      v[q] = (e < E) ? ls[tl * LLD + e] : -INFINITY;
-      if (e >= E) taken |= 1u << q;
+    route_one_token<EP>(ls + tl * LLD, E, k, lane, t, topk_idx, topk_w);
+  }
+}
+
+// ------------------------------------------------------------- small T ---
+constexpr int SNST = 6;    // ring depth: ~100 KB of W_r in flight per CTA
+
+template <int EP, int TSV>
+struct SmallCfg {
+  static constexpr int HC = 4096 / EP;                       // 16 KB of W_r per stage
+  static constexpr int TL = (TSV < 256 / EP) ? TSV : 256 / EP;  // token groups
+  static constexpr int TPT = TSV / TL;                       // tokens per thread
+  static constexpr int NTH = EP * TL;                        // threads
+  static constexpr int ring = SNST * (HC * EP * 4 + TSV * HC * 2);
+  static constexpr int bytes = ring + HC * TSV * 4;           // + FP32 x of one chunk
+};
+
+// TSV tokens per CTA (1, 2, 4 or 8): thread (g, e) owns expert e for the TPT
+// tokens g*TPT .. g*TPT+TPT-1 of the CTA.
+template <int EP, int TSV>
+__global__ void __launch_bounds__(SmallCfg<EP, TSV>::NTH) route_small_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
+    int T, int H, int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  using C = SmallCfg<EP, TSV>;
+  constexpr int HC = C::HC, TPT = C::TPT, NTH = C::NTH;
+  extern __shared__ float4 smem_f4[];
+  float* ws = reinterpret_cast<float*>(smem_f4);                    // [SNST][HC][EP]
+  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + SNST * HC * EP); // [SNST][TSV][HC]
+  float* xs = reinterpret_cast<float*>(xst + SNST * TSV * HC);      // [HC][TSV] FP32
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int e = tid % EP, g = tid / EP;
+  const int t0 = blockIdx.x * TSV;
+  const int nchunks = H / HC;
+
+  if (E < EP) {
+    for (int i = tid; i < SNST * HC * EP; i += NTH)
+      if ((i % EP) >= E) ws[i] = 0.0f;
+  }
+  auto issue_chunk = [&](int c) {
+    if (c < nchunks) {
+      const int buf = c % SNST;
+      const int h0 = c * HC;
+      float* wdst = ws + buf * HC * EP;
+      const float* wsrc = wr + (size_t)h0 * E;
+      if (E == EP) {
+        for (int i = tid; i < HC * EP / 4; i += NTH) cp_async_16(wdst + 4 * i, wsrc + 4 * i, 16);
+      } else {
+        for (int i = tid; i < HC * E; i += NTH)
+          cp_async_4(wdst + (i / E) * EP + (i % E), wsrc + i);
+      }
+      constexpr int PPR = HC / 8;  // 16-byte pieces per x row
+      uint16_t* xdst = xst + buf * TSV * HC;
+      for (int i = tid; i < TSV * PPR; i += NTH) {
+        const int r = i / PPR, pc = i % PPR;
+        const int t = t0 + r;
+        const uint16_t* src = (t < T) ? x + (size_t)t * H + h0 + 8 * pc : x;
+        cp_async_16(xdst + r * HC + 8 * pc, src, (t < T) ? 16 : 0);
+      }
     }
-    float sel_l[kMaxK];
-    int sel_e[kMaxK];
+    cp_async_commit();
+  };
+
+  float acc[TPT];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < k) {
-        float bv = -INFINITY;
-        int be = 0x7FFFFFFF;
+  for (int i = 0; i < TPT; ++i) acc[i] = 0.0f;
 #pragma unroll
-        for (int q = 0; q < NV; ++q) {
-          const int e = lane + 32 * q;
-          if (!((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
-            bv = v[q];
-            be = e;
-          }
+  for (int c = 0; c < SNST - 1; ++c) issue_chunk(c);
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = c % SNST;
+    issue_chunk(c + SNST - 1);
+    cp_async_wait<SNST - 1>();
+    __syncthreads();
+    // x chunk widened to FP32, transposed: xs[h][token], a thread's tokens adjacent
+    const uint16_t* xsb = xst + buf * TSV * HC;
+    for (int i = tid; i < TSV * HC; i += NTH) {
+      const int r = i / HC, hh = i % HC;
+      xs[hh * TSV + r] = __uint_as_float((uint32_t)xsb[r * HC + hh] << 16);
+    }
+    __syncthreads();
+    const float* wsb = ws + buf * HC * EP;
+#pragma unroll 8
+    for (int hh = 0; hh < HC; ++hh) {
+      const float wv = wsb[hh * EP + e];
+      float xv[TPT];
+      if constexpr (TPT % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < TPT / 4; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(xs + hh * TSV + g * TPT + 4 * q);
+          xv[4 * q] = v.x;
+          xv[4 * q + 1] = v.y;
+          xv[4 * q + 2] = v.z;
+          xv[4 * q + 3] = v.w;
         }
+      } else {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-          const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-          if (ov > bv || (ov == bv && oe < be)) {
-            bv = ov;
-            be = oe;
-          }
-        }
-        sel_l[j] = bv;
-        sel_e[j] = be;
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        for (int i = 0; i < TPT; ++i) xv[i] = xs[hh * TSV + g * TPT + i];
       }
+#pragma unroll
+      for (int i = 0; i < TPT; ++i) acc[i] = fmaf(xv[i], wv, acc[i]);
     }
-    // softmax denominator over all E experts, max-shifted
-    const float m = sel_l[0];
-    float z = 0.0f;
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+  constexpr int LLD = EP + 1;
+  float* ls = ws;  // [TSV][LLD], over the drained ring
+  if (e < E) {
+    const float b = (bias != nullptr) ? __ldg(bias + e) : 0.0f;
 #pragma unroll
-    for (int q = 0; q < NV; ++q)
-      if (lane + 32 * q < E) z = __fadd_rn(z, expf(v[q] - m));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z = __fadd_rn(z, __shfl_xor_sync(0xFFFFFFFFu, z, off));
-    // selected probabilities, their left-to-right sum, renormalised weights
-    float p[kMaxK];
-    float S = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < k) {
-        p[j] = __fdiv_rn(expf(sel_l[j] - m), z);
-        S = __fadd_rn(S, p[j]);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < k && lane == j) {
-        topk_idx[(size_t)t * k + j] = sel_e[j];
-        topk_w[(size_t)t * k + j] = __fdiv_rn(p[j], S);
-      }
+    for (int i = 0; i < TPT; ++i) {
+      float l = acc[i];
+      if (bias != nullptr) l = __fadd_rn(l, b);
+      ls[(g * TPT + i) * LLD + e] = l;
     }
   }
+  __syncthreads();
+  for (int tl = warp; tl < TSV; tl += NTH / 32) {
+    const int t = t0 + tl;
+    if (t < T) route_one_token<EP>(ls + tl * LLD, E, k, lane, t, topk_idx, topk_w);
+  }
+}
+
+template <int EP, int TSV>
+cudaError_t launch_small(const void* x, const float* wr, const float* bias, int T, int H, int E,
+                         int k, int32_t* idx, float* w, cudaStream_t s) {
+  using C = SmallCfg<EP, TSV>;
+  static bool attr[64] = {};
+  int dv = 0;
+  cudaGetDevice(&dv);
+  if (dv < 64 && !attr[dv]) {
+    cudaError_t e = cudaFuncSetAttribute(route_small_kernel<EP, TSV>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::bytes);
+    if (e != cudaSuccess) return e;
+    attr[dv] = true;
+  }
+  route_small_kernel<EP, TSV><<<(T + TSV - 1) / TSV, C::NTH, C::bytes, s>>>(
+      static_cast<const uint16_t*>(x), wr, bias, T, H, E, k, idx, w);
+  return cudaGetLastError();
 }
 
 template <int EP>
 cudaError_t launch_ep(const void* x, const float* wr, const float* bias, int T, int H, int E, int k,
                       int32_t* idx, float* w, cudaStream_t s) {
-  constexpr int smem = RouteSmem<EP>::bytes;
+  if (T <= kRouteSmallMaxT) {
+    if (T == 1) return launch_small<EP, 1>(x, wr, bias, T, H, E, k, idx, w, s);
+    if (T == 2) return launch_small<EP, 2>(x, wr, bias, T, H, E, k, idx, w, s);
+    if (T <= 4) return launch_small<EP, 4>(x, wr, bias, T, H, E, k, idx, w, s);
+    return launch_small<EP, 8>(x, wr, bias, T, H, E, k, idx, w, s);
+  }
+  constexpr int smem = RouteCfg<EP>::bytes;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
