@@ -39,6 +39,19 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "routed tokens/s per MoE layer fwd"
+
+# DRAM bytes per launch of the gate/up GEMM on the large workload, from one ncu
+# capture (profiles/gemm_dram_traffic_large.md), valid while the kernel sources
+# are unchanged since the capture.
+GEMM_TRAFFIC_LARGE = {"bytes": 15184053760 + 1074163456, "sources_sha256_16": "04154435aa06698f"}
+
+
+def gemm_sources_hash():
+    import hashlib
+    csrc = os.path.join(ROOT, "moe_expert_layer_fp32_gb300", "csrc")
+    data = b"".join(open(os.path.join(csrc, f), "rb").read()
+                    for f in ("expert_gemm.cu", "common.cuh"))
+    return hashlib.sha256(data).hexdigest()[:16]
 UNIT = "routed tokens/s"
 
 
@@ -372,7 +385,13 @@ def run_ours(args):
     achieved = gate_up_flop / (stage_ms["gemm_gate_up_swiglu"] / 1e3) / 1e12
     roofline = {"kernel": "grouped GEMM gate/up + SwiGLU (tcgen05)", "bound": "tensor",
                 "achieved": achieved, "peak": bf16_burst, "unit": "TFLOP/s",
-                "frac": achieved / bf16_burst, "traffic": None,
+                "frac": achieved / bf16_burst,
+                "traffic": (GEMM_TRAFFIC_LARGE["bytes"]
+                            if wl.name == "large" and gemm_sources_hash()
+                            == GEMM_TRAFFIC_LARGE["sources_sha256_16"] else None),
+                "traffic_note": "DRAM read+write bytes per launch, ncu capture "
+                                "(profiles/gemm_dram_traffic_large.md); algorithmic "
+                                f"{(4.0 * E * H * I + R * H * 2 + R * I * 2) / 1e9:.2f} GB",
                 "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)" if src == "measured"
                 else "fallback bf16 burst",
                 "algorithmic": f"4*R*H*I = {gate_up_flop:.4g} FLOP per launch"}
