@@ -208,6 +208,15 @@ moe_status moe_load_stats_noalloc(const int32_t* topk_idx, moe_dims d, int32_t* 
  * clears it. */
 moe_status moe_read_device_status(void* workspace, int32_t* status_out, void* stream);
 
+/* Diagnostics: the limit, in SM clock cycles, of every bounded wait inside the
+ * grouped GEMM kernels of calls launched afterwards (process-wide; cycles <= 0
+ * restores the default of 4e9, about 2 s).  A wait that runs out records
+ * MOE_ERR_TIMEOUT in the workspace status word; the kernel then waits for its own
+ * copies and MMAs in flight (always with the default limit), releases its tensor
+ * memory and exits, leaving the outputs of that call undefined and the CUDA
+ * context usable.  Meant for exercising that path, not for production. */
+moe_status moe_set_wait_limit(long long cycles);
+
 /* Static text for a status code. */
 const char* moe_status_string(moe_status s);
 

@@ -32,7 +32,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 ABI_SYMBOLS = ("moe_workspace_bytes", "moe_packed_weight_bytes", "moe_route", "moe_load_stats",
                "moe_load_summary_host", "moe_permute", "moe_prepack_expert_weights",
                "moe_expert_ffn", "moe_combine", "moe_layer_fwd", "moe_layer_fwd_profiled",
-               "moe_read_device_status", "moe_status_string", "moe_load_stats_noalloc")
+               "moe_read_device_status", "moe_status_string", "moe_load_stats_noalloc",
+               "moe_set_wait_limit")
 
 
 class moe_dims(ctypes.Structure):
@@ -65,6 +66,7 @@ _sig = {
     "moe_read_device_status": (ctypes.c_int, [_vp, _vp, _vp]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_load_stats_noalloc": (ctypes.c_int, [_vp, moe_dims, _vp, _vp, _vp, _vp]),
+    "moe_set_wait_limit": (ctypes.c_int, [ctypes.c_longlong]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -189,6 +191,11 @@ def moe_layer_fwd_profiled(x, w_router, bias, packed_weights, d, out, topk_idx_o
         _ptr(x), _ptr(w_router), _ptr(bias), _ptr(packed_weights), d, _ptr(out),
         _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), wp, wb, _stream(stream), arr,
         len(events)))
+
+
+def moe_set_wait_limit(cycles: int) -> None:
+    """Diagnostics: bounded-wait limit of the GEMM kernels (<= 0: default)."""
+    _check("moe_set_wait_limit", _lib.moe_set_wait_limit(int(cycles)))
 
 
 def moe_read_device_status(workspace, stream=None) -> int:

@@ -44,9 +44,10 @@
 // The tile shape, K order (k-blocks ascending, 16-wide MMAs ascending) and N
 // split depend only on H and I, never on T: batch-invariant by construction.
 //
-// Every wait is bounded (clock64 limit); a wait that runs out raises a CTA-wide
-// abort flag and records MOE_ERR_TIMEOUT; the roles then drain their own
-// in-flight TMA copies and MMAs (bounded again) before TMEM is released, and
+// Every wait is bounded (clock64 limit, spin_limit); a wait that runs out raises a
+// CTA-wide abort flag and records MOE_ERR_TIMEOUT; the roles then drain their own
+// in-flight TMA copies and MMAs (bounded by the fixed default limit, whatever
+// spin_limit is) before TMEM is released, and
 // the two CTAs of a cluster meet at a cluster barrier before either exits.
 #include "common.cuh"
 #include "kernels.cuh"
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(192, 1)
       if (aborted) {
         // the copies issued into the last STAGES slots may still be in flight
         for (int i = (it > C::STAGES ? it - C::STAGES : 0); i < it; ++i)
-          wait_drain(&full[i % C::STAGES], (i / C::STAGES) & 1, spin_limit);
+          wait_drain(&full[i % C::STAGES], (i / C::STAGES) & 1, kSpinLimitCycles);
       }
     }
   } else if (warp == 1) {
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       // every MMA this thread issued completes before TMEM is released
       mma_commit(mma_done);
-      wait_drain(mma_done, 0, spin_limit);
+      wait_drain(mma_done, 0, kSpinLimitCycles);
     }
   } else {
     // -------------------------------------------------------------- epilogue

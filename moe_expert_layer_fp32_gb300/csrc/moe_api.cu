@@ -7,6 +7,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -25,6 +27,9 @@ int device_sm_count() {
 }
 
 namespace {
+
+// Limit of the GEMM kernels' bounded waits, in SM clock cycles (diagnostics knob).
+std::atomic<long long> g_wait_limit{kSpinLimitCycles};
 
 // ------------------------------------------------------------------ layout ---
 constexpr size_t kAlign = 256;
@@ -181,9 +186,10 @@ moe_status do_expert_ffn(const void* x_perm, const int32_t* offsets, const void*
   const GemmOperand mb{w1, (uint64_t)d.H, (uint64_t)d.E * 2 * d.I};
   const GemmOperand mh{h, (uint64_t)d.I, (uint64_t)R};
   const GemmOperand md{w2, (uint64_t)d.I, (uint64_t)d.E * d.H};
-  MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, d.E, R, d.H, d.I, h, status, kSpinLimitCycles, s));
+  MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, d.E, R, d.H, d.I, h, status, g_wait_limit.load(), s));
   if (after_gate_up != nullptr) MOE_CUDA(cudaEventRecord(after_gate_up, s));
-  MOE_CUDA(launch_gemm_down(mh, md, offsets, d.E, R, d.H, d.I, y, status, kSpinLimitCycles, s));
+  MOE_CUDA(launch_gemm_down(mh, md, offsets, d.E, R, d.H, d.I, y, status, g_wait_limit.load(),
+                            s));
   return MOE_OK;
 }
 
@@ -398,6 +404,11 @@ moe_status moe_layer_fwd_profiled(const void* x, const float* w_router, const fl
   }
   return layer_fwd(x, w_router, bias, packed_weights, d, out, topk_idx_out, topk_w_out, counts_out,
                    workspace, ws_bytes, as_stream(stream), ev);
+}
+
+moe_status moe_set_wait_limit(long long cycles) {
+  g_wait_limit.store(cycles > 0 ? cycles : kSpinLimitCycles);
+  return MOE_OK;
 }
 
 moe_status moe_read_device_status(void* workspace, int32_t* status_out, void* stream) {
