@@ -54,8 +54,13 @@ def _L():
         lib.oracle_combine.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32]
         lib.oracle_layer_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp,
                                          vp, vp, i32]
+        lib.oracle_route_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, i32]
+        lib.oracle_combine_scaled.argtypes = [vp, vp, vp, ctypes.c_float, i32, i32, i32, vp, i32]
+        lib.oracle_exp_cw.argtypes = [ctypes.c_float]
+        lib.oracle_exp_cw.restype = ctypes.c_float
         for f in ("oracle_router_logits", "oracle_route", "oracle_load_stats", "oracle_permute",
-                  "oracle_expert_ffn", "oracle_combine", "oracle_layer_fwd"):
+                  "oracle_expert_ffn", "oracle_combine", "oracle_layer_fwd", "oracle_route_ex",
+                  "oracle_combine_scaled"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -100,6 +105,42 @@ def route(x, wr, bias, k, nthreads=0):
     _check(_L().oracle_route(_p(x), _p(wr), _p(bias), T, H, E, k, _p(idx), _p(w), nthreads),
            "route")
     return idx, w
+
+
+ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
+
+
+def route_ex(x, wr, bias, k, kind=ROUTER_SOFTMAX, weights_bf16=False, nthreads=0):
+    """Router variants: kind 0 softmax (bias joins the logits); kind 1 sigmoid
+    scores with `bias` as a selection-only correction bias.  weights_bf16 rounds
+    every weight to bf16."""
+    x = _c(x, np.uint16)
+    wr = _c(wr, np.float32)
+    bias = None if bias is None else _c(bias, np.float32)
+    T, H = x.shape
+    E = wr.shape[1]
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    _check(_L().oracle_route_ex(_p(x), _p(wr), _p(bias), int(kind), int(bool(weights_bf16)), T, H,
+                                E, k, _p(idx), _p(w), nthreads), "route_ex")
+    return idx, w
+
+
+def exp_cw(x: float) -> float:
+    return float(_L().oracle_exp_cw(float(x)))
+
+
+def combine_scaled(y, w, row_of_slot, scale, nthreads=0):
+    """out [T, H] bf16 bits, every routing weight multiplied by `scale` first."""
+    y = _c(y, np.float32)
+    w = _c(w, np.float32)
+    ros = _c(row_of_slot, np.int32).reshape(-1)
+    T, k = w.shape
+    H = y.shape[1]
+    out = np.empty((T, H), dtype=np.uint16)
+    _check(_L().oracle_combine_scaled(_p(y), _p(w), _p(ros), float(scale), T, H, k, _p(out),
+                                      nthreads), "combine_scaled")
+    return out
 
 
 def load_stats(idx, E):

@@ -133,6 +133,61 @@ void route_token(const float* l, int E, int k, int32_t* idx, float* w) {
 
 inline float silu(float g) { return g / (1.0f + std::exp(-g)); }
 
+// exp(x) in FP32 by Cody & Waite argument reduction and a Taylor polynomial:
+//   n = rint(x * log2 e),  r = x - n*ln2 (ln2 split in a high part with 16 significant
+//   bits, so n*LN2_HI is exact, plus the low remainder),  exp(r) = sum_{i<=7} r^i/i!
+//   evaluated by Horner with fused multiply-adds,  result = exp(r) * 2^n.
+// Every step is an IEEE FP32 operation, so the result is the same bits on any
+// machine that computes it the same way.  |r| <= ln2/2 keeps the truncated
+// series below half an FP32 ulp.
+float exp_cw(float x) {
+  if (x > 89.0f) x = 89.0f;
+  if (x < -104.0f) x = -104.0f;
+  const float LOG2E = 1.44269502162933349609375f;  // log2(e) rounded to FP32
+  const float LN2_HI = 0.693145751953125f;         // ln 2 to 16 significant bits
+  const float LN2_LO = 1.428606765330187e-06f;     // ln 2 - LN2_HI
+  const float n = std::rint(x * LOG2E);
+  float r = std::fma(-n, LN2_HI, x);
+  r = std::fma(-n, LN2_LO, r);
+  const float c[8] = {1.0f, 1.0f, 1.0f / 2, 1.0f / 6, 1.0f / 24, 1.0f / 120, 1.0f / 720,
+                      1.0f / 5040};
+  float p = c[7];
+  for (int i = 6; i >= 0; --i) p = std::fma(p, r, c[i]);
+  return std::ldexp(p, (int)n);
+}
+
+// Logistic sigmoid built on exp_cw: 1 / (1 + exp(-l)).
+inline float sigmoid_cw(float l) { return 1.0f / (1.0f + exp_cw(-l)); }
+
+// Round an FP32 value to bf16 (nearest, ties to even) and widen it back.
+inline float round_bf16(float f) { return bf16_to_f32(f32_to_bf16(f)); }
+
+// Router variant with GLM's choice rule ("0 train-infer mismatch", section
+// "Choosing GLM's eight experts"): sigmoid scores s_e = sigmoid(l_e); the FP32
+// correction bias joins only the selection key s_e + b_e (ties to the lower
+// index); the weights are the selected pre-bias scores divided by their sum
+// (added left to right, FP32).
+void route_token_sigmoid(const float* l, const float* corr_bias, int E, int k, int32_t* idx,
+                         float* w) {
+  std::vector<float> sc(E), key(E);
+  for (int e = 0; e < E; ++e) {
+    sc[e] = sigmoid_cw(l[e]);
+    key[e] = corr_bias ? sc[e] + corr_bias[e] : sc[e];
+  }
+  std::vector<int> order(E);
+  for (int e = 0; e < E; ++e) order[e] = e;
+  std::sort(order.begin(), order.end(), [&](int a, int b) {
+    if (key[a] != key[b]) return key[a] > key[b];
+    return a < b;
+  });
+  float S = 0.0f;
+  for (int j = 0; j < k; ++j) S = S + sc[order[j]];
+  for (int j = 0; j < k; ++j) {
+    idx[j] = order[j];
+    w[j] = sc[order[j]] / S;
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -156,6 +211,33 @@ int oracle_route(const uint16_t* x, const float* wr, const float* bias, int T, i
     std::vector<float> l(E);
     token_logits(x + t * H, wr, bias, H, E, l.data());
     route_token(l.data(), E, k, idx + t * k, w + t * k);
+  });
+  return 0;
+}
+
+// exp_cw for tests (pinned against the float64 exponential).
+float oracle_exp_cw(float x) { return exp_cw(x); }
+
+// Router with options:
+//   kind 0: softmax router (as oracle_route; `bias` joins the logits);
+//   kind 1: sigmoid scores, `bias` is GLM's correction bias used only for selection,
+//           weights = selected scores over their sum.
+//   weights_bf16 != 0: each final weight is rounded to bf16 (stored as its FP32 value).
+int oracle_route_ex(const uint16_t* x, const float* wr, const float* bias, int kind,
+                    int weights_bf16, int T, int H, int E, int k, int32_t* idx, float* w,
+                    int nthreads) {
+  if (T < 0 || H <= 0 || E <= 0 || k < 1 || k > E || kind < 0 || kind > 1) return 1;
+  parallel_for(T, nthreads, [&](int64_t t) {
+    std::vector<float> l(E);
+    if (kind == 0) {
+      token_logits(x + t * H, wr, bias, H, E, l.data());
+      route_token(l.data(), E, k, idx + t * k, w + t * k);
+    } else {
+      token_logits(x + t * H, wr, nullptr, H, E, l.data());
+      route_token_sigmoid(l.data(), bias, E, k, idx + t * k, w + t * k);
+    }
+    if (weights_bf16)
+      for (int j = 0; j < k; ++j) w[t * k + j] = round_bf16(w[t * k + j]);
   });
   return 0;
 }
@@ -266,6 +348,25 @@ int oracle_combine(const float* y, const float* w, const int32_t* row_of_slot, i
       for (int j = 0; j < k; ++j) {
         int64_t r = row_of_slot[t * k + j];
         acc = std::fma(w[t * k + j], y[r * H + c], acc);
+      }
+      out[t * H + c] = f32_to_bf16(acc);
+    }
+  });
+  return 0;
+}
+
+// Combine with a routing scale (GLM's factor applied inside the expert kernel):
+// each slot's weight is first multiplied by `scale` in FP32 (one rounding), then
+// the slot-order FMA chain runs as in oracle_combine.
+int oracle_combine_scaled(const float* y, const float* w, const int32_t* row_of_slot, float scale,
+                          int T, int H, int k, uint16_t* out, int nthreads) {
+  if (T < 0 || H <= 0 || k < 1) return 1;
+  parallel_for(T, nthreads, [&](int64_t t) {
+    for (int c = 0; c < H; ++c) {
+      float acc = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        int64_t r = row_of_slot[t * k + j];
+        acc = std::fma(scale * w[t * k + j], y[r * H + c], acc);
       }
       out[t * H + c] = f32_to_bf16(acc);
     }

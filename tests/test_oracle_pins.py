@@ -395,3 +395,87 @@ def test_layer_equals_composition_and_tiny_workload_sane():
     o = f32(out).astype(np.float64)
     assert np.abs(o - ref).max() <= 2e-2
     assert np.linalg.norm(o - ref) <= 5e-3 * np.linalg.norm(ref)
+
+
+# ------------------------------------------------------ router variants ---
+def test_exp_cw_matches_float64_exp():
+    """Cody-Waite + degree-7 Taylor exp: within 2^-23 relative of the float64
+    exponential over the range sigmoid scores use; exact at 0."""
+    import math
+    assert oracle.exp_cw(0.0) == 1.0
+    for v in np.linspace(-80.0, 80.0, 4001):
+        v = float(np.float32(v))
+        ref = math.exp(v)
+        assert abs(oracle.exp_cw(v) - ref) <= 2.0 ** -23 * ref, v
+
+
+def test_sigmoid_router_bias_only_selects():
+    """GLM's rule: the correction bias changes which experts are chosen but the
+    weights come from the pre-bias sigmoid scores, normalised over the chosen.
+    Catches a bias added to the weights, a softmax instead of the sigmoid, a
+    missing renormalisation."""
+    import math
+    x = bf16_bits([[1.0]])
+    wr = np.array([[0.0, 1.0, 2.0, 3.0]], np.float32)  # logits 0, 1, 2, 3
+    sig = [1 / (1 + math.exp(-v)) for v in (0.0, 1.0, 2.0, 3.0)]
+    idx, w = oracle.route_ex(x, wr, None, 2, kind=oracle.ROUTER_SIGMOID)
+    assert idx.tolist() == [[3, 2]]
+    np.testing.assert_allclose(w[0], [sig[3] / (sig[3] + sig[2]), sig[2] / (sig[3] + sig[2])],
+                               rtol=1e-6)
+    bias = np.array([1.0, 0.0, 0.0, 0.0], np.float32)
+    idx, w = oracle.route_ex(x, wr, bias, 2, kind=oracle.ROUTER_SIGMOID)
+    assert idx.tolist() == [[0, 3]]  # keys 1.5, .73, .88, .95
+    np.testing.assert_allclose(w[0], [sig[0] / (sig[0] + sig[3]), sig[3] / (sig[0] + sig[3])],
+                               rtol=1e-6)
+    # the softmax router instead adds the bias to the logits: 1, 1, 2, 3 -> [3, 2]
+    idx, _ = oracle.route_ex(x, wr, bias, 2, kind=oracle.ROUTER_SOFTMAX)
+    assert idx.tolist() == [[3, 2]]
+
+
+def test_sigmoid_router_ties_and_sums():
+    """Equal keys go to the lower index; weights sum to one; random inputs agree
+    with a float64 restatement of the rule up to FP32 rounding."""
+    T, H, E, k = 200, 32, 16, 4
+    x, wr = _tie_heavy_router(T, H, E, seed=3)
+    l = oracle.router_logits(x, wr).astype(np.float64)
+    bias = (synth.uniform_i32(3, synth.TID_MISC, (E,), -2, 3) * 0.125).astype(np.float32)
+    idx, w = oracle.route_ex(x, wr, bias, k, kind=oracle.ROUTER_SIGMOID)
+    s = 1.0 / (1.0 + np.exp(-l))
+    for t in range(T):
+        key = s[t] + bias
+        order = sorted(range(E), key=lambda e: (-key[e], e))
+        # keys equal in float64 are equal in FP32 here (coarse grids), so the order is pinned
+        if len(set(np.round(key, 6))) == E:
+            assert idx[t].tolist() == order[:k]
+        sel = s[t][idx[t]]
+        np.testing.assert_allclose(w[t], sel / sel.sum(), rtol=2e-6)
+    assert np.all(np.abs(w.astype(np.float64).sum(1) - 1) <= k * 2.0 ** -23)
+
+
+def test_weights_bf16_flag_rounds_each_weight():
+    """weights_bf16: every weight is the round-to-nearest-even bf16 of the FP32
+    weight (for both router kinds)."""
+    wl = synth.Workload("p", T=64, H=64, E=16, k=4, I=64, w_std=0.02, zipf_s=1.0)
+    x = synth.tokens(wl)
+    wr, b = synth.router(wl)
+    for kind in (oracle.ROUTER_SOFTMAX, oracle.ROUTER_SIGMOID):
+        i32, w32 = oracle.route_ex(x, wr * 10, b, wl.k, kind=kind)
+        i16, w16 = oracle.route_ex(x, wr * 10, b, wl.k, kind=kind, weights_bf16=True)
+        np.testing.assert_array_equal(i16, i32)
+        np.testing.assert_array_equal(w16, f32(f32_to_bf16_bits(w32)))
+
+
+def test_combine_scaled_closed_form():
+    """Scale 1 reproduces the plain combine; scale 2.5 with k = 1, w = 1 gives
+    bf16(2.5 y); the scale multiplies each weight before the FMA chain."""
+    T, H, k, R = 16, 24, 3, 48
+    y = synth.normal_f32(4, synth.TID_Y, (R, H), 1.0)
+    w = synth.uniform_f32(4, synth.TID_TOPK_W, (T, k), 0.0, 1.0)
+    ros = np.random.default_rng(1).permutation(R).astype(np.int32).reshape(T, k)
+    np.testing.assert_array_equal(oracle.combine_scaled(y, w, ros, 1.0), oracle.combine(y, w, ros))
+    one = oracle.combine_scaled(y[:T], np.ones((T, 1), np.float32), np.arange(T, dtype=np.int32),
+                                2.5)
+    np.testing.assert_array_equal(one, f32_to_bf16_bits((np.float32(2.5) * y[:T]).astype(np.float32)))
+    ref = np.einsum("tk,tkh->th", 2.5 * w.astype(np.float64), y[ros].astype(np.float64))
+    got = f32(oracle.combine_scaled(y, w, ros, 2.5)).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
