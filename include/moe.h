@@ -78,6 +78,29 @@ typedef struct {
   int32_t T, H, E, k, I;
 } moe_dims;
 
+/* Router variants ("0 train-infer mismatch for open-weight MoE RL"). */
+typedef enum {
+  /* FP32 softmax over the logits (plus the optional per-expert bias), top-k by
+   * logit, ties to the lower expert, left-to-right renormalisation
+   * (section "The router"). */
+  MOE_ROUTER_SOFTMAX = 0,
+  /* GLM's rule (section "Choosing GLM's eight experts"): scores s = sigmoid(l);
+   * the FP32 correction bias is added only to choose the top k (ties to the lower
+   * expert); the weights are the chosen pre-bias scores divided by their sum
+   * (added left to right, FP32).  The exponential is Cody & Waite reduction with a
+   * degree-7 Taylor polynomial in FP32 fused multiply-adds, so the choice is
+   * reproducible bit for bit on any implementation of the same steps. */
+  MOE_ROUTER_SIGMOID_BIAS_SELECT = 1
+} moe_router_kind;
+
+typedef struct {
+  int32_t kind;          /* moe_router_kind */
+  int32_t weights_bf16;  /* nonzero: every routing weight is rounded to bf16 (section
+                            "The router": the renormalised weights are cast to BF16) */
+  float route_scale;     /* > 0: multiplies every routing weight in FP32 inside the
+                            combine (GLM applies 2.5 inside the expert kernel); 1 = none */
+} moe_router_opts;
+
 /* Bytes of device workspace that every call taking a workspace needs for these
  * dimensions (the full layer's need; each step uses a part of the same layout).
  * The workspace must be 256-byte aligned and its first 256 bytes (the status
@@ -103,6 +126,13 @@ size_t moe_packed_weight_bytes(moe_dims d);
  * with it to a few FP32 ulp (the exponential differs between math libraries). */
 moe_status moe_route(const void* x, const float* w_router, const float* bias, moe_dims d,
                      int32_t* topk_idx, float* topk_w, void* stream);
+
+/* moe_route with a router variant (opts NULL: softmax, FP32 weights).
+ * opts->route_scale is not used here (it belongs to the combine).  An unknown
+ * kind or a scale that is not a positive finite number: MOE_ERR_INVALID_ARG. */
+moe_status moe_route_ex(const void* x, const float* w_router, const float* bias,
+                        const moe_router_opts* opts, moe_dims d, int32_t* topk_idx, float* topk_w,
+                        void* stream);
 
 /* Step: per-expert load.  counts[e] = number of (t, j) with topk_idx[t,j] = e;
  * offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e] (so offsets[E] = T*k).
@@ -156,6 +186,11 @@ moe_status moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void
 moe_status moe_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, moe_dims d,
                        void* out, void* stream);
 
+/* moe_combine with every routing weight multiplied by route_scale (FP32, one
+ * rounding) before the slot-order chain; route_scale = 1 is moe_combine. */
+moe_status moe_combine_ex(const float* y, const float* topk_w, const int32_t* row_of_slot,
+                          float route_scale, moe_dims d, void* out, void* stream);
+
 /* The whole layer forward: route -> load stats -> permute -> expert FFN ->
  * combine, enqueued on one stream with no host synchronisation.
  *   x [T, H] bf16; w_router [H, E] fp32; bias [E] fp32 or NULL; packed_weights
@@ -166,6 +201,14 @@ moe_status moe_layer_fwd(const void* x, const float* w_router, const float* bias
                          const void* packed_weights, moe_dims d, void* out, int32_t* topk_idx_out,
                          float* topk_w_out, int32_t* counts_out, void* workspace, size_t ws_bytes,
                          void* stream);
+
+/* moe_layer_fwd with a router variant and routing scale (opts NULL: the defaults
+ * of moe_layer_fwd).  For MOE_ROUTER_SIGMOID_BIAS_SELECT, `bias` is the
+ * selection-only correction bias. */
+moe_status moe_layer_fwd_ex(const void* x, const float* w_router, const float* bias,
+                            const moe_router_opts* opts, const void* packed_weights, moe_dims d,
+                            void* out, int32_t* topk_idx_out, float* topk_w_out,
+                            int32_t* counts_out, void* workspace, size_t ws_bytes, void* stream);
 
 /* moe_layer_fwd that also records caller-created CUDA events (cudaEvent_t
  * passed as void*) on `stream` at the step boundaries, for per-step timing:

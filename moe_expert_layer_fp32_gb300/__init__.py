@@ -33,7 +33,7 @@ ABI_SYMBOLS = ("moe_workspace_bytes", "moe_packed_weight_bytes", "moe_route", "m
                "moe_load_summary_host", "moe_permute", "moe_prepack_expert_weights",
                "moe_expert_ffn", "moe_combine", "moe_layer_fwd", "moe_layer_fwd_profiled",
                "moe_read_device_status", "moe_status_string", "moe_load_stats_noalloc",
-               "moe_set_wait_limit")
+               "moe_set_wait_limit", "moe_route_ex", "moe_combine_ex", "moe_layer_fwd_ex")
 
 
 class moe_dims(ctypes.Structure):
@@ -46,6 +46,22 @@ class moe_dims(ctypes.Structure):
 
 def dims(T, H, E, k, I) -> moe_dims:
     return moe_dims(T, H, E, k, I)
+
+
+MOE_ROUTER_SOFTMAX, MOE_ROUTER_SIGMOID_BIAS_SELECT = 0, 1
+
+
+class moe_router_opts(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("weights_bf16", ctypes.c_int32),
+                ("route_scale", ctypes.c_float)]
+
+
+def router_opts(kind=MOE_ROUTER_SOFTMAX, weights_bf16=False, route_scale=1.0) -> moe_router_opts:
+    return moe_router_opts(int(kind), int(bool(weights_bf16)), float(route_scale))
+
+
+def _opts(o):
+    return None if o is None else ctypes.byref(o)
 
 
 _vp, _sz, _i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
@@ -67,6 +83,10 @@ _sig = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_load_stats_noalloc": (ctypes.c_int, [_vp, moe_dims, _vp, _vp, _vp, _vp]),
     "moe_set_wait_limit": (ctypes.c_int, [ctypes.c_longlong]),
+    "moe_route_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, moe_dims, _vp, _vp, _vp]),
+    "moe_combine_ex": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, moe_dims, _vp, _vp]),
+    "moe_layer_fwd_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, moe_dims, _vp, _vp, _vp, _vp,
+                                        _vp, _sz, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -119,6 +139,25 @@ def moe_packed_weight_bytes(d: moe_dims) -> int:
 def moe_route(x, w_router, bias, d, topk_idx, topk_w, stream=None):
     _check("moe_route", _lib.moe_route(_ptr(x), _ptr(w_router), _ptr(bias), d, _ptr(topk_idx),
                                        _ptr(topk_w), _stream(stream)))
+
+
+def moe_route_ex(x, w_router, bias, opts, d, topk_idx, topk_w, stream=None):
+    _check("moe_route_ex", _lib.moe_route_ex(_ptr(x), _ptr(w_router), _ptr(bias), _opts(opts), d,
+                                             _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+
+
+def moe_combine_ex(y, topk_w, row_of_slot, route_scale, d, out, stream=None):
+    _check("moe_combine_ex", _lib.moe_combine_ex(_ptr(y), _ptr(topk_w), _ptr(row_of_slot),
+                                                 float(route_scale), d, _ptr(out),
+                                                 _stream(stream)))
+
+
+def moe_layer_fwd_ex(x, w_router, bias, opts, packed_weights, d, out, topk_idx_out, topk_w_out,
+                     counts_out, workspace, stream=None):
+    wp, wb = _ws(workspace)
+    _check("moe_layer_fwd_ex", _lib.moe_layer_fwd_ex(
+        _ptr(x), _ptr(w_router), _ptr(bias), _opts(opts), _ptr(packed_weights), d, _ptr(out),
+        _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), wp, wb, _stream(stream)))
 
 
 def moe_load_stats(topk_idx, d, counts, offsets, workspace, stream=None):
@@ -223,8 +262,10 @@ def prepack(w_gate, w_up, w_down, d, stream=None) -> torch.Tensor:
     return packed
 
 
-def layer_forward(x, w_router, bias, packed, d, workspace, stream=None, want_routing=False):
-    """out [T, H] bf16 (and topk_idx, topk_w, counts if want_routing)."""
+def layer_forward(x, w_router, bias, packed, d, workspace, stream=None, want_routing=False,
+                  opts=None):
+    """out [T, H] bf16 (and topk_idx, topk_w, counts if want_routing).  opts: a
+    moe_router_opts (router variant, bf16 weights, routing scale) or None."""
     dev = x.device
     out = torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev)
     idx = w = counts = None
@@ -232,7 +273,7 @@ def layer_forward(x, w_router, bias, packed, d, workspace, stream=None, want_rou
         idx = torch.empty((d.T, d.k), dtype=torch.int32, device=dev)
         w = torch.empty((d.T, d.k), dtype=torch.float32, device=dev)
         counts = torch.empty(d.E, dtype=torch.int32, device=dev)
-    moe_layer_fwd(x, w_router, bias, packed, d, out, idx, w, counts, workspace, stream)
+    moe_layer_fwd_ex(x, w_router, bias, opts, packed, d, out, idx, w, counts, workspace, stream)
     return (out, idx, w, counts) if want_routing else out
 
 

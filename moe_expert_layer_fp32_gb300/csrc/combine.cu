@@ -7,6 +7,10 @@
 // before the single rounding.  Here: acc = 0, acc = fmaf(w[t,j], y[row_j, c], acc)
 // for j = 0..k-1, out = bf16(acc).
 //
+// An optional routing scale (GLM applies 2.5 inside the expert kernel) multiplies
+// each weight once in FP32 before the chain; a scale of 1 leaves the weights, and
+// so the result, unchanged.
+//
 // Memory-bound gather: one CTA per token, 16-byte loads of the k FP32 rows
 // (all issued before the FMA chain), 8-byte stores of four bf16 outputs.
 #include "common.cuh"
@@ -18,7 +22,7 @@ namespace {
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ y,
                                                       const float* __restrict__ topk_w,
                                                       const int32_t* __restrict__ row_of_slot,
-                                                      int T, int H, int k,
+                                                      int T, int H, int k, float scale,
                                                       uint16_t* __restrict__ out) {
   __shared__ int s_row[kMaxK];
   __shared__ float s_w[kMaxK];
@@ -27,7 +31,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   if (threadIdx.x < k) {
     const int r = row_of_slot[(size_t)t * k + threadIdx.x];
     s_row[threadIdx.x] = (r >= 0 && r < R) ? r : -1;
-    s_w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+    s_w[threadIdx.x] = __fmul_rn(scale, topk_w[(size_t)t * k + threadIdx.x]);
   }
   __syncthreads();
   int row[kMaxK];
@@ -62,9 +66,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 }  // namespace
 
 cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, int T,
-                           int H, int k, void* out, cudaStream_t s) {
+                           int H, int k, float scale, void* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<T, 128, 0, s>>>(y, topk_w, row_of_slot, T, H, k, static_cast<uint16_t*>(out));
+  combine_kernel<<<T, 128, 0, s>>>(y, topk_w, row_of_slot, T, H, k, scale,
+                                   static_cast<uint16_t*>(out));
   return cudaGetLastError();
 }
 

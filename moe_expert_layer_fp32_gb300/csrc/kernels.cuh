@@ -14,9 +14,12 @@ constexpr int kPermBlock = 256;  // tokens per ranking block of the permutation
 constexpr long long kSpinLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int kRouteSmallMaxT = 64;  // batches up to this size use the small-T router kernel
 
-// router: projection (FP32 FMA chain), softmax, top-k, renormalisation
+// router: projection (FP32 FMA chain), then kind 0: softmax, top-k (bias joins the
+// logits); kind 1: sigmoid scores, top-k on score + correction bias, weights from
+// the scores.  weights_bf16 rounds every weight to bf16.
 cudaError_t launch_route(const void* x, const float* w_router, const float* bias, int T, int H,
-                         int E, int k, int32_t* topk_idx, float* topk_w, cudaStream_t s);
+                         int E, int k, int kind, int weights_bf16, int32_t* topk_idx,
+                         float* topk_w, cudaStream_t s);
 
 // per-block expert counts: blk_counts [nb, E], nb = ceil(T / kPermBlock)
 cudaError_t launch_block_counts(const int32_t* topk_idx, int T, int k, int E, int32_t* blk_counts,
@@ -70,9 +73,9 @@ cudaError_t launch_gemm_down(const GemmOperand& a, const GemmOperand& b,
 // N tile width of the down projection for this H (fixed per model shape)
 int gemm_down_bn(int H);
 
-// out[t] = bf16(slot-order FMA chain of topk_w[t,j] * y[row_of_slot[t*k+j]])
+// out[t] = bf16(slot-order FMA chain of (scale * topk_w[t,j]) * y[row_of_slot[t*k+j]])
 cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, int T,
-                           int H, int k, void* out, cudaStream_t s);
+                           int H, int k, float scale, void* out, cudaStream_t s);
 
 // number of SMs of the current device (cached per device)
 int device_sm_count();

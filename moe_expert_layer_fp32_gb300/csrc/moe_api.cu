@@ -193,11 +193,21 @@ moe_status do_expert_ffn(const void* x_perm, const int32_t* offsets, const void*
   return MOE_OK;
 }
 
+moe_status check_opts(const moe_router_opts& o) {
+  if (o.kind != MOE_ROUTER_SOFTMAX && o.kind != MOE_ROUTER_SIGMOID_BIAS_SELECT)
+    return MOE_ERR_INVALID_ARG;
+  if (!(o.route_scale > 0.0f) || !isfinite(o.route_scale)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+constexpr moe_router_opts kDefaultOpts = {MOE_ROUTER_SOFTMAX, 0, 1.0f};
+
 moe_status layer_fwd(const void* x, const float* w_router, const float* bias,
-                     const void* packed_weights, const moe_dims& d, void* out,
-                     int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out,
+                     const moe_router_opts& opts, const void* packed_weights, const moe_dims& d,
+                     void* out, int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out,
                      void* workspace, size_t ws_bytes, cudaStream_t s, cudaEvent_t* ev) {
   MOE_TRY(check_dims(d));
+  MOE_TRY(check_opts(opts));
   MOE_TRY(check_ws(d, workspace, ws_bytes));
   MOE_TRY(need(w_router));
   if (bias != nullptr) MOE_TRY(need(bias));
@@ -224,7 +234,8 @@ moe_status layer_fwd(const void* x, const float* w_router, const float* bias,
     return MOE_OK;
   };
   MOE_TRY(mark(0));
-  MOE_CUDA(launch_route(x, w_router, bias, d.T, d.H, d.E, d.k, idx, w, s));
+  MOE_CUDA(launch_route(x, w_router, bias, d.T, d.H, d.E, d.k, opts.kind, opts.weights_bf16, idx,
+                        w, s));
   MOE_TRY(mark(1));
   if (d.T > 0 && d.T <= kPermBlock) {
     // one ranking block: counts, offsets and ranks in a single launch
@@ -244,7 +255,7 @@ moe_status layer_fwd(const void* x, const float* w_router, const float* bias,
   else
     MOE_TRY(mark(4));
   MOE_TRY(mark(5));
-  if (d.T > 0) MOE_CUDA(launch_combine(y, w, ros, d.T, d.H, d.k, out, s));
+  if (d.T > 0) MOE_CUDA(launch_combine(y, w, ros, d.T, d.H, d.k, opts.route_scale, out, s));
   MOE_TRY(mark(6));
   return MOE_OK;
 }
@@ -280,9 +291,12 @@ const char* moe_status_string(moe_status s) {
   return "unknown status";
 }
 
-moe_status moe_route(const void* x, const float* w_router, const float* bias, moe_dims d,
-                     int32_t* topk_idx, float* topk_w, void* stream) {
+moe_status moe_route_ex(const void* x, const float* w_router, const float* bias,
+                        const moe_router_opts* opts, moe_dims d, int32_t* topk_idx, float* topk_w,
+                        void* stream) {
+  const moe_router_opts o = opts ? *opts : kDefaultOpts;
   MOE_TRY(check_dims(d));
+  MOE_TRY(check_opts(o));
   if (d.T == 0) return MOE_OK;
   MOE_TRY(need(x));
   MOE_TRY(need(w_router));
@@ -290,8 +304,14 @@ moe_status moe_route(const void* x, const float* w_router, const float* bias, mo
   MOE_TRY(need(topk_idx));
   MOE_TRY(need(topk_w));
   MOE_TRY(device_ok());
-  MOE_CUDA(launch_route(x, w_router, bias, d.T, d.H, d.E, d.k, topk_idx, topk_w, as_stream(stream)));
+  MOE_CUDA(launch_route(x, w_router, bias, d.T, d.H, d.E, d.k, o.kind, o.weights_bf16, topk_idx,
+                        topk_w, as_stream(stream)));
   return MOE_OK;
+}
+
+moe_status moe_route(const void* x, const float* w_router, const float* bias, moe_dims d,
+                     int32_t* topk_idx, float* topk_w, void* stream) {
+  return moe_route_ex(x, w_router, bias, nullptr, d, topk_idx, topk_w, stream);
 }
 
 moe_status moe_load_stats(const int32_t* topk_idx, moe_dims d, int32_t* counts, int32_t* offsets,
@@ -367,25 +387,41 @@ moe_status moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void
   return do_expert_ffn(x_perm, offsets, packed_weights, d, y, workspace, as_stream(stream));
 }
 
-moe_status moe_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, moe_dims d,
-                       void* out, void* stream) {
+moe_status moe_combine_ex(const float* y, const float* topk_w, const int32_t* row_of_slot,
+                          float route_scale, moe_dims d, void* out, void* stream) {
   MOE_TRY(check_dims(d));
+  if (!(route_scale > 0.0f) || !isfinite(route_scale)) return MOE_ERR_INVALID_ARG;
   if (d.T == 0) return MOE_OK;
   MOE_TRY(need(y));
   MOE_TRY(need(topk_w));
   MOE_TRY(need(row_of_slot));
   MOE_TRY(need(out));
   MOE_TRY(device_ok());
-  MOE_CUDA(launch_combine(y, topk_w, row_of_slot, d.T, d.H, d.k, out, as_stream(stream)));
+  MOE_CUDA(launch_combine(y, topk_w, row_of_slot, d.T, d.H, d.k, route_scale, out,
+                          as_stream(stream)));
   return MOE_OK;
+}
+
+moe_status moe_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, moe_dims d,
+                       void* out, void* stream) {
+  return moe_combine_ex(y, topk_w, row_of_slot, 1.0f, d, out, stream);
 }
 
 moe_status moe_layer_fwd(const void* x, const float* w_router, const float* bias,
                          const void* packed_weights, moe_dims d, void* out, int32_t* topk_idx_out,
                          float* topk_w_out, int32_t* counts_out, void* workspace, size_t ws_bytes,
                          void* stream) {
-  return layer_fwd(x, w_router, bias, packed_weights, d, out, topk_idx_out, topk_w_out, counts_out,
-                   workspace, ws_bytes, as_stream(stream), nullptr);
+  return layer_fwd(x, w_router, bias, kDefaultOpts, packed_weights, d, out, topk_idx_out, topk_w_out,
+                   counts_out, workspace, ws_bytes, as_stream(stream), nullptr);
+}
+
+moe_status moe_layer_fwd_ex(const void* x, const float* w_router, const float* bias,
+                            const moe_router_opts* opts, const void* packed_weights, moe_dims d,
+                            void* out, int32_t* topk_idx_out, float* topk_w_out,
+                            int32_t* counts_out, void* workspace, size_t ws_bytes, void* stream) {
+  return layer_fwd(x, w_router, bias, opts ? *opts : kDefaultOpts, packed_weights, d, out,
+                   topk_idx_out, topk_w_out, counts_out, workspace, ws_bytes, as_stream(stream),
+                   nullptr);
 }
 
 moe_status moe_layer_fwd_profiled(const void* x, const float* w_router, const float* bias,
@@ -402,8 +438,8 @@ moe_status moe_layer_fwd_profiled(const void* x, const float* w_router, const fl
     if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
     ev[i] = static_cast<cudaEvent_t>(events[i]);
   }
-  return layer_fwd(x, w_router, bias, packed_weights, d, out, topk_idx_out, topk_w_out, counts_out,
-                   workspace, ws_bytes, as_stream(stream), ev);
+  return layer_fwd(x, w_router, bias, kDefaultOpts, packed_weights, d, out, topk_idx_out, topk_w_out,
+                   counts_out, workspace, ws_bytes, as_stream(stream), ev);
 }
 
 moe_status moe_set_wait_limit(long long cycles) {

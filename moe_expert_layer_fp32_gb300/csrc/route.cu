@@ -63,20 +63,67 @@ __device__ __forceinline__ int expert_of(int lane, int jj) {
   }
 }
 
-// One warp routes token t from its E logits lrow[0..E) (shared memory): top-k by
-// (logit desc, expert asc), FP32 softmax over all E, renormalised weights.
-template <int EP>
-__device__ __forceinline__ void route_one_token(const float* lrow, int E, int k, int lane, int t,
+// exp(x) in FP32 by Cody & Waite argument reduction and a Taylor polynomial of
+// degree 7 (Horner, fused multiply-adds), scaled by 2^n: n = rint(x log2 e),
+// r = x - n ln2 with ln2 split into a 16-bit high part and its remainder.  Every
+// step is one IEEE FP32 operation, so any implementation of the same steps gives
+// the same bits (used where the exponential decides which experts are chosen).
+__device__ __forceinline__ float exp_cw(float x) {
+  x = fminf(fmaxf(x, -104.0f), 89.0f);
+  const float LOG2E = 1.44269502162933349609375f;
+  const float LN2_HI = 0.693145751953125f;
+  const float LN2_LO = 1.428606765330187e-06f;
+  const float n = rintf(__fmul_rn(x, LOG2E));
+  float r = fmaf(-n, LN2_HI, x);
+  r = fmaf(-n, LN2_LO, r);
+  float p = 1.0f / 5040.0f;
+  p = fmaf(p, r, 1.0f / 720.0f);
+  p = fmaf(p, r, 1.0f / 120.0f);
+  p = fmaf(p, r, 1.0f / 24.0f);
+  p = fmaf(p, r, 1.0f / 6.0f);
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  return ldexpf(p, (int)n);
+}
+
+__device__ __forceinline__ float round_bf16(float f) {
+  return __bfloat162float(__float2bfloat16_rn(f));
+}
+
+// One warp routes token t from its E logits lrow[0..E) (shared memory).
+//   KIND 0 (softmax): top-k by (logit desc, expert asc), FP32 softmax over all E,
+//     selected probabilities renormalised left to right.
+//   KIND 1 (sigmoid, "0 train-infer mismatch", section "Choosing GLM's eight
+//     experts"): scores s = sigmoid(l); the correction bias joins only the
+//     selection key s + b (ties to the lower expert); weights = selected s over
+//     their left-to-right sum.
+// wbf16 rounds every final weight to bf16.
+template <int EP, int KIND>
+__device__ __forceinline__ void route_one_token(const float* lrow, const float* corr_bias, int E,
+                                                int k, int wbf16, int lane, int t,
                                                 int32_t* __restrict__ topk_idx,
                                                 float* __restrict__ topk_w) {
   constexpr int NV = EP / 32;
-  float v[NV];
+  float v[NV];   // selection key
+  float sc[NV];  // KIND 1: pre-bias scores
   unsigned taken = 0;
 #pragma unroll
   for (int q = 0; q < NV; ++q) {
     const int e = lane + 32 * q;
-    v[q] = (e < E) ? lrow[e] : -INFINITY;
-    if (e >= E) taken |= 1u << q;
+    if (e < E) {
+      if constexpr (KIND == 0) {
+        v[q] = lrow[e];
+        sc[q] = 0.0f;
+      } else {
+        sc[q] = __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_cw(-lrow[e])));
+        v[q] = (corr_bias != nullptr) ? __fadd_rn(sc[q], __ldg(corr_bias + e)) : sc[q];
+      }
+    } else {
+      v[q] = -INFINITY;
+      sc[q] = 0.0f;
+      taken |= 1u << q;
+    }
   }
   float sel_l[kMaxK];
   int sel_e[kMaxK];
@@ -102,43 +149,62 @@ __device__ __forceinline__ void route_one_token(const float* lrow, int E, int k,
           be = oe;
         }
       }
+      if constexpr (KIND == 1) {
+        // the winner's pre-bias score, from the lane that owns expert be
+        float mine = 0.0f;
+#pragma unroll
+        for (int q = 0; q < NV; ++q)
+          if (q == (be >> 5)) mine = sc[q];
+        bv = __shfl_sync(0xFFFFFFFFu, mine, be & 31);
+      }
       sel_l[j] = bv;
       sel_e[j] = be;
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
     }
   }
-  // softmax denominator over all E experts, max-shifted
-  const float m = sel_l[0];
-  float z = 0.0f;
-#pragma unroll
-  for (int q = 0; q < NV; ++q)
-    if (lane + 32 * q < E) z = __fadd_rn(z, expf(v[q] - m));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) z = __fadd_rn(z, __shfl_xor_sync(0xFFFFFFFFu, z, off));
-  // selected probabilities, their left-to-right sum, renormalised weights
   float p[kMaxK];
   float S = 0.0f;
+  if constexpr (KIND == 0) {
+    // softmax denominator over all E experts, max-shifted
+    const float m = sel_l[0];
+    float z = 0.0f;
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j < k) {
-      p[j] = __fdiv_rn(expf(sel_l[j] - m), z);
-      S = __fadd_rn(S, p[j]);
+    for (int q = 0; q < NV; ++q)
+      if (lane + 32 * q < E) z = __fadd_rn(z, expf(v[q] - m));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z = __fadd_rn(z, __shfl_xor_sync(0xFFFFFFFFu, z, off));
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < k) {
+        p[j] = __fdiv_rn(expf(sel_l[j] - m), z);
+        S = __fadd_rn(S, p[j]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < k) {
+        p[j] = sel_l[j];
+        S = __fadd_rn(S, p[j]);
+      }
     }
   }
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
     if (j < k && lane == j) {
+      float wj = __fdiv_rn(p[j], S);
+      if (wbf16) wj = round_bf16(wj);
       topk_idx[(size_t)t * k + j] = sel_e[j];
-      topk_w[(size_t)t * k + j] = __fdiv_rn(p[j], S);
+      topk_w[(size_t)t * k + j] = wj;
     }
   }
 }
 
-template <int EP>
+template <int EP, int KIND>
 __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restrict__ x,
                                                         const float* __restrict__ wr,
                                                         const float* __restrict__ bias, int T,
-                                                        int H, int E, int k,
+                                                        int H, int E, int k, int wbf16,
                                                         int32_t* __restrict__ topk_idx,
                                                         float* __restrict__ topk_w) {
   using C = RouteCfg<EP>;
@@ -248,17 +314,18 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
   }
   cp_async_wait<0>();
 
-  // ---- epilogue: logits (+ bias) to shared memory --------------------------
+  // ---- epilogue: logits (+ bias for the softmax router) to shared memory ---
   constexpr int LLD = EP + 1;
+  const bool add_bias = KIND == 0 && bias != nullptr;
   float* ls = reinterpret_cast<float*>(smem_f4);  // [BT][LLD], over the drained ring
 #pragma unroll
   for (int j = 0; j < TE; ++j) {
     const int e = expert_of<EP>(lane, j);
-    const float b = (bias != nullptr && e < E) ? __ldg(bias + e) : 0.0f;
+    const float b = (add_bias && e < E) ? __ldg(bias + e) : 0.0f;
 #pragma unroll
     for (int i = 0; i < TT; ++i) {
       float l = acc[i][j];
-      if (bias != nullptr) l = __fadd_rn(l, b);
+      if (add_bias) l = __fadd_rn(l, b);
       ls[(warp * TT + i) * LLD + e] = l;
     }
   }
@@ -267,7 +334,8 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
     const int tl = warp * TT + i;
     const int t = t0 + tl;
     if (t >= T) break;
-    route_one_token<EP>(ls + tl * LLD, E, k, lane, t, topk_idx, topk_w);
+    route_one_token<EP, KIND>(ls + tl * LLD, KIND == 1 ? bias : nullptr, E, k, wbf16, lane, t,
+                              topk_idx, topk_w);
   }
 }
 
@@ -286,10 +354,11 @@ struct SmallCfg {
 
 // TSV tokens per CTA (1, 2, 4 or 8): thread (g, e) owns expert e for the TPT
 // tokens g*TPT .. g*TPT+TPT-1 of the CTA.
-template <int EP, int TSV>
+template <int EP, int TSV, int KIND>
 __global__ void __launch_bounds__(SmallCfg<EP, TSV>::NTH) route_small_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
-    int T, int H, int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+    int T, int H, int E, int k, int wbf16, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w) {
   using C = SmallCfg<EP, TSV>;
   constexpr int HC = C::HC, TPT = C::TPT, NTH = C::NTH;
   extern __shared__ float4 smem_f4[];
@@ -372,74 +441,87 @@ __global__ void __launch_bounds__(SmallCfg<EP, TSV>::NTH) route_small_kernel(
   cp_async_wait<0>();
   constexpr int LLD = EP + 1;
   float* ls = ws;  // [TSV][LLD], over the drained ring
+  const bool add_bias = KIND == 0 && bias != nullptr;
   if (e < E) {
-    const float b = (bias != nullptr) ? __ldg(bias + e) : 0.0f;
+    const float b = add_bias ? __ldg(bias + e) : 0.0f;
 #pragma unroll
     for (int i = 0; i < TPT; ++i) {
       float l = acc[i];
-      if (bias != nullptr) l = __fadd_rn(l, b);
+      if (add_bias) l = __fadd_rn(l, b);
       ls[(g * TPT + i) * LLD + e] = l;
     }
   }
   __syncthreads();
   for (int tl = warp; tl < TSV; tl += NTH / 32) {
     const int t = t0 + tl;
-    if (t < T) route_one_token<EP>(ls + tl * LLD, E, k, lane, t, topk_idx, topk_w);
+    if (t < T)
+      route_one_token<EP, KIND>(ls + tl * LLD, KIND == 1 ? bias : nullptr, E, k, wbf16, lane, t,
+                                topk_idx, topk_w);
   }
 }
 
-template <int EP, int TSV>
+template <int EP, int TSV, int KIND>
 cudaError_t launch_small(const void* x, const float* wr, const float* bias, int T, int H, int E,
-                         int k, int32_t* idx, float* w, cudaStream_t s) {
+                         int k, int wbf16, int32_t* idx, float* w, cudaStream_t s) {
   using C = SmallCfg<EP, TSV>;
   static bool attr[64] = {};
   int dv = 0;
   cudaGetDevice(&dv);
   if (dv < 64 && !attr[dv]) {
-    cudaError_t e = cudaFuncSetAttribute(route_small_kernel<EP, TSV>,
+    cudaError_t e = cudaFuncSetAttribute(route_small_kernel<EP, TSV, KIND>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::bytes);
     if (e != cudaSuccess) return e;
     attr[dv] = true;
   }
-  route_small_kernel<EP, TSV><<<(T + TSV - 1) / TSV, C::NTH, C::bytes, s>>>(
-      static_cast<const uint16_t*>(x), wr, bias, T, H, E, k, idx, w);
+  route_small_kernel<EP, TSV, KIND><<<(T + TSV - 1) / TSV, C::NTH, C::bytes, s>>>(
+      static_cast<const uint16_t*>(x), wr, bias, T, H, E, k, wbf16, idx, w);
   return cudaGetLastError();
 }
 
-template <int EP>
+template <int EP, int KIND>
 cudaError_t launch_ep(const void* x, const float* wr, const float* bias, int T, int H, int E, int k,
-                      int32_t* idx, float* w, cudaStream_t s) {
+                      int wbf16, int32_t* idx, float* w, cudaStream_t s) {
   if (T <= kRouteSmallMaxT) {
-    if (T == 1) return launch_small<EP, 1>(x, wr, bias, T, H, E, k, idx, w, s);
-    if (T == 2) return launch_small<EP, 2>(x, wr, bias, T, H, E, k, idx, w, s);
-    if (T <= 4) return launch_small<EP, 4>(x, wr, bias, T, H, E, k, idx, w, s);
-    return launch_small<EP, 8>(x, wr, bias, T, H, E, k, idx, w, s);
+    if (T == 1) return launch_small<EP, 1, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    if (T == 2) return launch_small<EP, 2, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    if (T <= 4) return launch_small<EP, 4, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    return launch_small<EP, 8, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
   }
   constexpr int smem = RouteCfg<EP>::bytes;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel<EP>,
+    cudaError_t e = cudaFuncSetAttribute(route_kernel<EP, KIND>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   dim3 grid((T + BT - 1) / BT);
-  route_kernel<EP><<<grid, NTHR, smem, s>>>(static_cast<const uint16_t*>(x), wr, bias, T, H, E,
-                                            k, idx, w);
+  route_kernel<EP, KIND><<<grid, NTHR, smem, s>>>(static_cast<const uint16_t*>(x), wr, bias, T, H,
+                                                  E, k, wbf16, idx, w);
   return cudaGetLastError();
+}
+
+template <int KIND>
+cudaError_t launch_kind(const void* x, const float* w_router, const float* bias, int T, int H,
+                        int E, int k, int wbf16, int32_t* topk_idx, float* topk_w, cudaStream_t s) {
+  if (E <= 32) return launch_ep<32, KIND>(x, w_router, bias, T, H, E, k, wbf16, topk_idx, topk_w, s);
+  if (E <= 64) return launch_ep<64, KIND>(x, w_router, bias, T, H, E, k, wbf16, topk_idx, topk_w, s);
+  if (E <= 128)
+    return launch_ep<128, KIND>(x, w_router, bias, T, H, E, k, wbf16, topk_idx, topk_w, s);
+  return launch_ep<256, KIND>(x, w_router, bias, T, H, E, k, wbf16, topk_idx, topk_w, s);
 }
 
 }  // namespace
 
 cudaError_t launch_route(const void* x, const float* w_router, const float* bias, int T, int H,
-                         int E, int k, int32_t* topk_idx, float* topk_w, cudaStream_t s) {
+                         int E, int k, int kind, int weights_bf16, int32_t* topk_idx,
+                         float* topk_w, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  if (E <= 32) return launch_ep<32>(x, w_router, bias, T, H, E, k, topk_idx, topk_w, s);
-  if (E <= 64) return launch_ep<64>(x, w_router, bias, T, H, E, k, topk_idx, topk_w, s);
-  if (E <= 128) return launch_ep<128>(x, w_router, bias, T, H, E, k, topk_idx, topk_w, s);
-  return launch_ep<256>(x, w_router, bias, T, H, E, k, topk_idx, topk_w, s);
+  if (kind == 1)
+    return launch_kind<1>(x, w_router, bias, T, H, E, k, weights_bf16, topk_idx, topk_w, s);
+  return launch_kind<0>(x, w_router, bias, T, H, E, k, weights_bf16, topk_idx, topk_w, s);
 }
 
 }  // namespace moe
