@@ -56,6 +56,13 @@ def _L():
                                          vp, vp, i32]
         lib.oracle_route_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, i32]
         lib.oracle_combine_scaled.argtypes = [vp, vp, vp, ctypes.c_float, i32, i32, i32, vp, i32]
+        lib.oracle_weighted_counts.argtypes = [vp, vp, i32, i32, i32, vp]
+        lib.oracle_lpt_placement.argtypes = [vp, i32, i32, vp, vp]
+        lib.oracle_rank_metrics.argtypes = [vp, i32, vp, vp]
+        lib.oracle_permute_remap.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
+        for f in ("oracle_weighted_counts", "oracle_lpt_placement", "oracle_rank_metrics",
+                  "oracle_permute_remap"):
+            getattr(lib, f).restype = ctypes.c_int
         lib.oracle_exp_cw.argtypes = [ctypes.c_float]
         lib.oracle_exp_cw.restype = ctypes.c_float
         for f in ("oracle_router_logits", "oracle_route", "oracle_load_stats", "oracle_permute",
@@ -124,6 +131,52 @@ def route_ex(x, wr, bias, k, kind=ROUTER_SOFTMAX, weights_bf16=False, nthreads=0
     _check(_L().oracle_route_ex(_p(x), _p(wr), _p(bias), int(kind), int(bool(weights_bf16)), T, H,
                                 E, k, _p(idx), _p(w), nthreads), "route_ex")
     return idx, w
+
+
+def weighted_counts(idx, q, E):
+    """int64 [E]: assignments of expert e counted q[t] times (multiplicity weights)."""
+    idx = _c(idx, np.int32)
+    q = _c(q, np.int32)
+    T, k = idx.shape
+    out = np.empty(E, dtype=np.int64)
+    _check(_L().oracle_weighted_counts(_p(idx), _p(q), T, k, E, _p(out)), "weighted_counts")
+    return out
+
+
+def lpt_placement(loads, P):
+    """(slot_of_expert [E] int32, rank_loads [P] int64): layer-local LPT placement."""
+    loads = _c(loads, np.int64)
+    E = loads.shape[0]
+    pi = np.empty(E, dtype=np.int32)
+    G = np.empty(P, dtype=np.int64)
+    _check(_L().oracle_lpt_placement(_p(loads), E, P, _p(pi), _p(G)), "lpt_placement")
+    return pi, G
+
+
+def rank_metrics(G):
+    """(cv, eta_ep) of rank loads."""
+    G = _c(G, np.int64)
+    cv, eta = ctypes.c_double(), ctypes.c_double()
+    _check(_L().oracle_rank_metrics(_p(G), G.shape[0], ctypes.addressof(cv),
+                                    ctypes.addressof(eta)), "rank_metrics")
+    return cv.value, eta.value
+
+
+def permute_remap(x, idx, slot_of_expert, offsets, E, with_x_perm=True):
+    """permute with logical expert e dispatched to physical slot slot_of_expert[e]."""
+    x = _c(x, np.uint16)
+    idx = _c(idx, np.int32)
+    pi = _c(slot_of_expert, np.int32)
+    offsets = _c(offsets, np.int32)
+    T, H = x.shape
+    k = idx.shape[1]
+    R = T * k
+    x_perm = np.empty((R, H), dtype=np.uint16) if with_x_perm else None
+    ros = np.empty(R, dtype=np.int32)
+    sor = np.empty(R, dtype=np.int32)
+    _check(_L().oracle_permute_remap(_p(x), _p(idx), _p(pi), _p(offsets), T, H, E, k, _p(x_perm),
+                                     _p(ros), _p(sor)), "permute_remap")
+    return x_perm, ros, sor
 
 
 def exp_cw(x: float) -> float:

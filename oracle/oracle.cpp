@@ -268,6 +268,74 @@ int oracle_load_stats(const int32_t* idx, int T, int k, int E, int32_t* counts, 
   return 0;
 }
 
+// "HARTS", Eq. 20 and section "MoE execution and objectives": compact row t stands
+// for q[t] semantic tokens; its assignments count q[t] times in the expert loads
+// while routing and compute run once.  out[e] = sum over (t, j) with idx[t,j] = e
+// of q[t] (int64).
+int oracle_weighted_counts(const int32_t* idx, const int32_t* q, int T, int k, int E,
+                           int64_t* out) {
+  if (T < 0 || k < 1 || E <= 0) return 1;
+  for (int e = 0; e < E; ++e) out[e] = 0;
+  for (int64_t t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      int e = idx[t * k + j];
+      if (e < 0 || e >= E) return 2;
+      out[e] += q[t];
+    }
+  return 0;
+}
+
+// "RoutePack", Algorithm 1 (layer-local LPT expert placement): experts in order
+// of (load descending, index ascending); each goes to the least-loaded rank
+// (ties: lower rank id) among ranks with a free slot; pi(e) = p*Hs + n_p, the
+// next slot of that rank.  P ranks of Hs = E/P slots.  Also returns the rank
+// loads G_p (Eq. 10).
+int oracle_lpt_placement(const int64_t* loads, int E, int P, int32_t* slot_of_expert,
+                         int64_t* rank_loads) {
+  if (E <= 0 || P <= 0 || E % P != 0) return 1;
+  const int Hs = E / P;
+  std::vector<int64_t> G(P, 0);
+  std::vector<int> n(P, 0);
+  std::vector<int> order(E);
+  for (int e = 0; e < E; ++e) order[e] = e;
+  std::sort(order.begin(), order.end(), [&](int a, int b) {
+    if (loads[a] != loads[b]) return loads[a] > loads[b];
+    return a < b;
+  });
+  for (int e : order) {
+    int best = -1;
+    for (int p = 0; p < P; ++p) {
+      if (n[p] >= Hs) continue;
+      if (best < 0 || G[p] < G[best]) best = p;  // ties keep the lower rank id
+    }
+    slot_of_expert[e] = best * Hs + n[best];
+    G[best] += loads[e];
+    n[best] += 1;
+  }
+  if (rank_loads)
+    for (int p = 0; p < P; ++p) rank_loads[p] = G[p];
+  return 0;
+}
+
+// Rank-load balance of one layer: coefficient of variation ("RoutePack", Eq. 22,
+// population form over the P ranks) and EP balance efficiency (Eq. 23 for one
+// row, layer and shard: mean rank load over the largest).
+int oracle_rank_metrics(const int64_t* G, int P, double* cv, double* eta) {
+  if (P <= 0) return 1;
+  double mean = 0.0, mx = 0.0;
+  for (int p = 0; p < P; ++p) {
+    mean += (double)G[p];
+    mx = std::max(mx, (double)G[p]);
+  }
+  mean /= P;
+  double var = 0.0;
+  for (int p = 0; p < P; ++p) var += ((double)G[p] - mean) * ((double)G[p] - mean);
+  var /= P;
+  *cv = mean > 0 ? std::sqrt(var) / mean : 0.0;
+  *eta = mx > 0 ? mean / mx : 1.0;
+  return 0;
+}
+
 // Step 5: stable permutation into expert-contiguous rows (reading R5).
 // Walk slots in token order, then slot order; each takes the next free row of its
 // expert.  slot s = t*k + j.  x_perm[r] is a byte copy of x[slot_of_row[r] / k].
@@ -288,6 +356,21 @@ int oracle_permute(const uint16_t* x, const int32_t* idx, const int32_t* offsets
     }
   }
   return 0;
+}
+
+// Step 5 with "RoutePack"'s dispatcher remap (section 3.3, Figure 4): the router's
+// logical expert e is dispatched to physical slot slot_of_expert[e]; rows are
+// grouped by physical slot (offsets indexed by slot), stable within a slot.
+int oracle_permute_remap(const uint16_t* x, const int32_t* idx, const int32_t* slot_of_expert,
+                         const int32_t* offsets, int T, int H, int E, int k, uint16_t* x_perm,
+                         int32_t* row_of_slot, int32_t* slot_of_row) {
+  std::vector<int32_t> phys((size_t)T * k);
+  for (int64_t s2 = 0; s2 < (int64_t)T * k; ++s2) {
+    int e = idx[s2];
+    if (e < 0 || e >= E) return 2;
+    phys[s2] = slot_of_expert[e];
+  }
+  return oracle_permute(x, phys.data(), offsets, T, H, E, k, x_perm, row_of_slot, slot_of_row);
 }
 
 // Steps 6-7: per expert e, rows [offsets[e], offsets[e+1]) of x_perm [R, H]:

@@ -479,3 +479,79 @@ def test_combine_scaled_closed_form():
     ref = np.einsum("tk,tkh->th", 2.5 * w.astype(np.float64), y[ros].astype(np.float64))
     got = f32(oracle.combine_scaled(y, w, ros, 2.5)).astype(np.float64)
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+
+
+# ------------------------------------- placement, rank loads, multiplicity ---
+def test_lpt_placement_hand_example():
+    """Algorithm 1 traced by hand: loads [10,9,8,7,1,1,1,1], 2 ranks of 4 slots.
+    Order e0..e7; e0->r0 (10), e1->r1 (9), e2->r1 (17), e3->r0 (17), e4 ties ->
+    r0 (18), e5->r1 (18), e6 ties -> r0 (19), e7->r1 (19).  Catches a wrong sort
+    key, a wrong tie rule, slots filled out of order, a missing capacity check."""
+    pi, G = oracle.lpt_placement([10, 9, 8, 7, 1, 1, 1, 1], 2)
+    assert pi.tolist() == [0, 4, 5, 1, 2, 6, 3, 7]
+    assert G.tolist() == [19, 19]
+
+
+def test_lpt_placement_invariants():
+    """Random loads: a permutation of slots, exactly E/P experts per rank, rank
+    loads = sums of their experts' loads (Eq. 10), the classic LPT bound
+    max G <= sum L / P + max L, and no worse than identity placement."""
+    rng = np.random.default_rng(0)
+    for E, P in [(64, 8), (128, 16), (256, 8), (12, 3)]:
+        loads = rng.zipf(1.5, E).astype(np.int64) * 100 + rng.integers(0, 50, E)
+        pi, G = oracle.lpt_placement(loads, P)
+        assert sorted(pi.tolist()) == list(range(E))
+        owner = pi // (E // P)
+        assert np.all(np.bincount(owner, minlength=P) == E // P)
+        np.testing.assert_array_equal(G, np.bincount(owner, weights=loads, minlength=P))
+        assert G.max() <= loads.sum() / P + loads.max()
+        ident = np.bincount(np.arange(E) // (E // P), weights=loads, minlength=P)
+        assert G.max() <= ident.max()
+
+
+def test_rank_metrics_closed_forms():
+    assert oracle.rank_metrics([5, 5, 5, 5]) == (0.0, 1.0)
+    cv, eta = oracle.rank_metrics([6, 2])  # mean 4, std 2, max 6
+    assert cv == pytest.approx(0.5) and eta == pytest.approx(4 / 6)
+
+
+def test_weighted_counts():
+    """q = 1 gives the plain counts; sum = k * sum(q); brute force."""
+    T, E, k = 100, 16, 4
+    idx = np.argsort(synth.uniform_f32(1, synth.TID_TOPK_IDX, (T, E), 0, 1), axis=1)[:, :k]
+    idx = idx.astype(np.int32)
+    c, _, _, _ = oracle.load_stats(idx, E)
+    np.testing.assert_array_equal(oracle.weighted_counts(idx, np.ones(T, np.int32), E), c)
+    q = synth.uniform_i32(1, synth.TID_MISC, (T,), 1, 9)
+    wc = oracle.weighted_counts(idx, q, E)
+    assert wc.sum() == k * q.sum()
+    ref = np.zeros(E, np.int64)
+    for t in range(T):
+        for e in idx[t]:
+            ref[e] += q[t]
+    np.testing.assert_array_equal(wc, ref)
+
+
+def test_permute_remap_groups_by_physical_slot():
+    """The dispatcher remap: rows grouped by physical slot pi(e), stable within a
+    slot; with the identity map it is the plain permutation."""
+    T, H, E, k = 90, 16, 8, 2
+    x = synth.normal_bf16(2, synth.TID_X, (T, H), 1.0)
+    wr = synth.normal_f32(2, synth.TID_WR, (H, E), 1.0)
+    idx, _ = oracle.route(x, wr, None, k)
+    c, off, _, _ = oracle.load_stats(idx, E)
+    ident = np.arange(E, dtype=np.int32)
+    a = oracle.permute(x, idx, off, E)
+    b = oracle.permute_remap(x, idx, ident, off, E)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
+    pi, _ = oracle.lpt_placement(c.astype(np.int64), 2)
+    phys_counts = np.zeros(E, np.int64)
+    phys_counts[pi] = c
+    poff = np.concatenate([[0], np.cumsum(phys_counts)]).astype(np.int32)
+    xp, ros, sor = oracle.permute_remap(x, idx, pi, poff, E)
+    for slot in range(E):
+        toks = sor[poff[slot]:poff[slot + 1]] // k
+        e = int(np.flatnonzero(pi == slot)[0])
+        assert np.all(np.diff(toks) > 0) and np.all((idx[toks] == e).any(axis=1))
+    np.testing.assert_array_equal(xp, x[sor // k])
