@@ -148,6 +148,45 @@ moe_status moe_load_stats(const int32_t* topk_idx, moe_dims d, int32_t* counts, 
 moe_status moe_load_summary_host(const int32_t* counts_host, int32_t E, double* imbalance,
                                  double* cv);
 
+/* moe_load_stats with two options:
+ *   slot_of_expert [E] (device, or NULL): "RoutePack" section 3.3 / Figure 4, the
+ *     dispatcher's map from the router's logical expert e to physical slot
+ *     slot_of_expert[e] (a permutation of 0..E-1, e.g. from
+ *     moe_lpt_placement_host).  counts and offsets are then indexed by physical
+ *     slot, the grouping the expert FFN runs in when its weights were packed with
+ *     the same map (moe_prepack_expert_weights_ex).  A map that is not a
+ *     permutation yields repeated slots within a token: flagged
+ *     (MOE_ERR_DEVICE_CHECK), rows stay inside [0, T*k).
+ *   q [T] int32 (device) and weighted_counts [E] int64 (device), both or neither:
+ *     "HARTS" Eq. 20, a compact row t standing for q[t] >= 0 tokens counts q[t]
+ *     times: weighted_counts[e] = sum of q[t] over the (t, j) routed to logical
+ *     expert e (integer atomics, exact).  Routing and compute are unaffected. */
+moe_status moe_load_stats_ex(const int32_t* topk_idx, const int32_t* slot_of_expert,
+                             const int32_t* q, moe_dims d, int32_t* counts, int32_t* offsets,
+                             int64_t* weighted_counts, void* workspace, size_t ws_bytes,
+                             void* stream);
+
+/* Host: "RoutePack" Algorithm 1, layer-local LPT expert placement.  Experts in
+ * order of (load descending, index ascending) each go to the least-loaded of the
+ * P ranks that still has a free slot (ties: lower rank), into that rank's next
+ * slot: slot_of_expert[e] = p * (E/P) + n_p.  rank_loads [P] (optional) receives
+ * the rank loads G_p of Eq. 10.  E must be a multiple of P and at most 256.
+ * All pointers are host pointers. */
+moe_status moe_lpt_placement_host(const int64_t* loads, int32_t E, int32_t P,
+                                  int32_t* slot_of_expert, int64_t* rank_loads);
+
+/* Host: balance of P rank loads ("RoutePack" Eq. 22, one layer: population
+ * std/mean; Eq. 23 for one row, layer and shard: mean/max).  Outputs may be NULL. */
+moe_status moe_rank_load_summary_host(const int64_t* rank_loads, int32_t P, double* cv,
+                                      double* eta_ep);
+
+/* moe_permute with the dispatcher's logical -> physical slot map (NULL: identity):
+ * rows are grouped by physical slot, stable within a slot; offsets are indexed
+ * by slot (as moe_load_stats_ex writes them with the same map). */
+moe_status moe_permute_ex(const void* x, const int32_t* topk_idx, const int32_t* slot_of_expert,
+                          const int32_t* offsets, moe_dims d, void* x_perm, int32_t* row_of_slot,
+                          int32_t* slot_of_row, void* workspace, size_t ws_bytes, void* stream);
+
 /* Step: dispatch.  Stable permutation into expert-contiguous rows: slot
  * s = t*k + j with expert e goes to row
  *   r = offsets[e] + #{ t' < t : token t' chose e },
@@ -166,6 +205,15 @@ moe_status moe_permute(const void* x, const int32_t* topk_idx, const int32_t* of
  *   packed: moe_packed_weight_bytes(d) bytes, 16-byte aligned. */
 moe_status moe_prepack_expert_weights(const void* w_gate, const void* w_up, const void* w_down,
                                       moe_dims d, void* packed, size_t packed_bytes, void* stream);
+
+/* moe_prepack_expert_weights with expert e packed into physical slot
+ * slot_of_expert[e] (device, or NULL for the identity): "RoutePack" Figure 4,
+ * each expert's weights materialised in its destination slot.  Slots outside
+ * [0, E) are not written. */
+moe_status moe_prepack_expert_weights_ex(const void* w_gate, const void* w_up,
+                                         const void* w_down, const int32_t* slot_of_expert,
+                                         moe_dims d, void* packed, size_t packed_bytes,
+                                         void* stream);
 
 /* Step: grouped SwiGLU experts.  For each expert e and each row r in
  * [offsets[e], offsets[e+1]):

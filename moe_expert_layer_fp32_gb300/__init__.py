@@ -33,7 +33,9 @@ ABI_SYMBOLS = ("moe_workspace_bytes", "moe_packed_weight_bytes", "moe_route", "m
                "moe_load_summary_host", "moe_permute", "moe_prepack_expert_weights",
                "moe_expert_ffn", "moe_combine", "moe_layer_fwd", "moe_layer_fwd_profiled",
                "moe_read_device_status", "moe_status_string", "moe_load_stats_noalloc",
-               "moe_set_wait_limit", "moe_route_ex", "moe_combine_ex", "moe_layer_fwd_ex")
+               "moe_set_wait_limit", "moe_route_ex", "moe_combine_ex", "moe_layer_fwd_ex",
+               "moe_load_stats_ex", "moe_lpt_placement_host", "moe_rank_load_summary_host",
+               "moe_permute_ex", "moe_prepack_expert_weights_ex")
 
 
 class moe_dims(ctypes.Structure):
@@ -87,6 +89,13 @@ _sig = {
     "moe_combine_ex": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, moe_dims, _vp, _vp]),
     "moe_layer_fwd_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, moe_dims, _vp, _vp, _vp, _vp,
                                         _vp, _sz, _vp]),
+    "moe_load_stats_ex": (ctypes.c_int, [_vp, _vp, _vp, moe_dims, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_lpt_placement_host": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp]),
+    "moe_rank_load_summary_host": (ctypes.c_int, [_vp, _i32, _vp, _vp]),
+    "moe_permute_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, moe_dims, _vp, _vp, _vp, _vp, _sz,
+                                      _vp]),
+    "moe_prepack_expert_weights_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, moe_dims, _vp, _sz,
+                                                     _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -172,6 +181,50 @@ def moe_load_stats_noalloc(topk_idx, d, counts, offsets, device_status=None, str
     for the size limit and the rule that overlapping calls race)."""
     _check("moe_load_stats_noalloc", _lib.moe_load_stats_noalloc(
         _ptr(topk_idx), d, _ptr(counts), _ptr(offsets), _ptr(device_status), _stream(stream)))
+
+
+def moe_load_stats_ex(topk_idx, slot_of_expert, q, d, counts, offsets, weighted_counts,
+                      workspace, stream=None):
+    wp, wb = _ws(workspace)
+    _check("moe_load_stats_ex", _lib.moe_load_stats_ex(
+        _ptr(topk_idx), _ptr(slot_of_expert), _ptr(q), d, _ptr(counts), _ptr(offsets),
+        _ptr(weighted_counts), wp, wb, _stream(stream)))
+
+
+def moe_lpt_placement_host(loads, P):
+    """(slot_of_expert [E] int32, rank_loads [P] int64) from host loads (RoutePack Alg. 1)."""
+    import numpy as np
+    L = np.ascontiguousarray(loads, dtype=np.int64)
+    pi = np.empty(L.size, dtype=np.int32)
+    G = np.empty(P, dtype=np.int64)
+    _check("moe_lpt_placement_host", _lib.moe_lpt_placement_host(
+        L.ctypes.data, int(L.size), int(P), pi.ctypes.data, G.ctypes.data))
+    return pi, G
+
+
+def moe_rank_load_summary_host(rank_loads):
+    """(cv, eta_ep) of host rank loads."""
+    import numpy as np
+    G = np.ascontiguousarray(rank_loads, dtype=np.int64)
+    cv, eta = ctypes.c_double(), ctypes.c_double()
+    _check("moe_rank_load_summary_host", _lib.moe_rank_load_summary_host(
+        G.ctypes.data, int(G.size), ctypes.addressof(cv), ctypes.addressof(eta)))
+    return cv.value, eta.value
+
+
+def moe_permute_ex(x, topk_idx, slot_of_expert, offsets, d, x_perm, row_of_slot, slot_of_row,
+                   workspace, stream=None):
+    wp, wb = _ws(workspace)
+    _check("moe_permute_ex", _lib.moe_permute_ex(
+        _ptr(x), _ptr(topk_idx), _ptr(slot_of_expert), _ptr(offsets), d, _ptr(x_perm),
+        _ptr(row_of_slot), _ptr(slot_of_row), wp, wb, _stream(stream)))
+
+
+def moe_prepack_expert_weights_ex(w_gate, w_up, w_down, slot_of_expert, d, packed, stream=None):
+    nbytes = packed.numel() * packed.element_size() if isinstance(packed, torch.Tensor) else 1 << 62
+    _check("moe_prepack_expert_weights_ex", _lib.moe_prepack_expert_weights_ex(
+        _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(slot_of_expert), d, _ptr(packed), nbytes,
+        _stream(stream)))
 
 
 def moe_load_summary_host(counts_host):

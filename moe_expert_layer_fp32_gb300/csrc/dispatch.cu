@@ -25,14 +25,21 @@ constexpr int PB = kPermBlock;  // 256 tokens, 8 warps
 // Builds masks[w][e] for the block's tokens; returns nothing but fills smem.
 // sidx holds the block's topk_idx rows.  Invalid ids and repeated experts within
 // one token are flagged and left out.
+// With `remap` (RoutePack's dispatcher map, logical expert -> physical slot),
+// sidx holds physical slots; out-of-range slots are flagged like bad ids.
 __device__ __forceinline__ void build_masks(const int32_t* __restrict__ topk_idx, int T, int k,
                                             int E, int t0, uint32_t* masks, int32_t* sidx,
-                                            int32_t* status) {
+                                            int32_t* status,
+                                            const int32_t* __restrict__ remap = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ntok = min(PB, T - t0);
   const int n = ntok * k;
   const int32_t* src = topk_idx + (size_t)t0 * k;
-  for (int i = tid; i < n; i += blockDim.x) sidx[i] = __ldg(src + i);
+  for (int i = tid; i < n; i += blockDim.x) {
+    int e = __ldg(src + i);
+    if (remap != nullptr && e >= 0 && e < E) e = __ldg(remap + e);
+    sidx[i] = e;
+  }
   for (int i = tid; i < 8 * E; i += blockDim.x) masks[i] = 0u;
   __syncthreads();
   const int tl = warp * 32 + lane;
@@ -53,12 +60,13 @@ __device__ __forceinline__ void build_masks(const int32_t* __restrict__ topk_idx
 __global__ void __launch_bounds__(PB) block_counts_kernel(const int32_t* __restrict__ topk_idx,
                                                           int T, int k, int E,
                                                           int32_t* __restrict__ blk_counts,
-                                                          int32_t* status) {
+                                                          int32_t* status,
+                                                          const int32_t* __restrict__ remap) {
   extern __shared__ uint32_t smem_u[];
   uint32_t* masks = smem_u;                               // [8][E]
   int32_t* sidx = reinterpret_cast<int32_t*>(smem_u + 8 * E);  // [PB*k]
   const int b = blockIdx.x;
-  build_masks(topk_idx, T, k, E, b * PB, masks, sidx, status);
+  build_masks(topk_idx, T, k, E, b * PB, masks, sidx, status, remap);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int c = 0;
 #pragma unroll
@@ -123,12 +131,13 @@ __global__ void __launch_bounds__(PB) rank_kernel(const int32_t* __restrict__ to
                                                   const int32_t* __restrict__ blk_base,
                                                   int32_t* __restrict__ row_of_slot,
                                                   int32_t* __restrict__ slot_of_row,
-                                                  int32_t* status) {
+                                                  int32_t* status,
+                                                  const int32_t* __restrict__ remap) {
   extern __shared__ uint32_t smem_u[];
   uint32_t* masks = smem_u;
   int32_t* sidx = reinterpret_cast<int32_t*>(smem_u + 8 * E);
   const int b = blockIdx.x, t0 = b * PB;
-  build_masks(topk_idx, T, k, E, t0, masks, sidx, status);
+  build_masks(topk_idx, T, k, E, t0, masks, sidx, status, remap);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tl = warp * 32 + lane;
   const int t = t0 + tl;
@@ -210,6 +219,35 @@ __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __res
   }
 }
 
+// "HARTS", Eq. 20: compact row t counts q[t] times in the expert loads.  Integer
+// additions only (order-free): shared-memory partial sums per block, then one
+// global atomic per expert and block.  out (int64 [E]) must start at zero.
+__global__ void __launch_bounds__(PB) weighted_counts_kernel(const int32_t* __restrict__ topk_idx,
+                                                             const int32_t* __restrict__ q, int T,
+                                                             int k, int E,
+                                                             unsigned long long* __restrict__ out,
+                                                             int32_t* status) {
+  __shared__ unsigned long long acc[kMaxE];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) acc[e] = 0ull;
+  __syncthreads();
+  const int t = blockIdx.x * PB + threadIdx.x;
+  if (t < T) {
+    const int qt = __ldg(q + t);
+    if (qt < 0) flag_error(status, MOE_ERR_DEVICE_CHECK);
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(topk_idx + (size_t)t * k + j);
+      if (e < 0 || e >= E || qt < 0) {
+        flag_error(status, MOE_ERR_DEVICE_CHECK);
+        continue;
+      }
+      atomicAdd(&acc[e], (unsigned long long)qt);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (acc[e] != 0ull) atomicAdd(out + e, acc[e]);
+}
+
 // One warp per token: read the row once (16-byte vectors), write it to its k rows.
 __global__ void __launch_bounds__(256) copy_rows_kernel(const uint16_t* __restrict__ x,
                                                         const int32_t* __restrict__ row_of_slot,
@@ -254,10 +292,11 @@ size_t mask_smem_bytes(int E, int k) { return (size_t)8 * E * 4 + (size_t)PB * k
 }  // namespace
 
 cudaError_t launch_block_counts(const int32_t* topk_idx, int T, int k, int E, int32_t* blk_counts,
-                                int32_t* status, cudaStream_t s) {
+                                int32_t* status, cudaStream_t s, const int32_t* remap) {
   if (T == 0) return cudaSuccess;
   const int nb = (T + PB - 1) / PB;
-  block_counts_kernel<<<nb, PB, mask_smem_bytes(E, k), s>>>(topk_idx, T, k, E, blk_counts, status);
+  block_counts_kernel<<<nb, PB, mask_smem_bytes(E, k), s>>>(topk_idx, T, k, E, blk_counts, status,
+                                                           remap);
   return cudaGetLastError();
 }
 
@@ -271,11 +310,20 @@ cudaError_t launch_scan(const int32_t* blk_counts, int nb, int E, int R, int32_t
 
 cudaError_t launch_rank(const int32_t* topk_idx, int T, int k, int E, const int32_t* blk_base,
                         int32_t* row_of_slot, int32_t* slot_of_row, int32_t* status,
-                        cudaStream_t s) {
+                        cudaStream_t s, const int32_t* remap) {
   if (T == 0) return cudaSuccess;
   const int nb = (T + PB - 1) / PB;
   rank_kernel<<<nb, PB, mask_smem_bytes(E, k), s>>>(topk_idx, T, k, E, blk_base, row_of_slot,
-                                                    slot_of_row, status);
+                                                    slot_of_row, status, remap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weighted_counts(const int32_t* topk_idx, const int32_t* q, int T, int k, int E,
+                                   int64_t* out, int32_t* status, cudaStream_t s) {
+  cudaError_t err = cudaMemsetAsync(out, 0, (size_t)E * sizeof(int64_t), s);
+  if (err != cudaSuccess || T == 0) return err;
+  weighted_counts_kernel<<<(T + PB - 1) / PB, PB, 0, s>>>(
+      topk_idx, q, T, k, E, reinterpret_cast<unsigned long long*>(out), status);
   return cudaGetLastError();
 }
 

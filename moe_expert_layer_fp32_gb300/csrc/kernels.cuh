@@ -22,8 +22,9 @@ cudaError_t launch_route(const void* x, const float* w_router, const float* bias
                          float* topk_w, cudaStream_t s);
 
 // per-block expert counts: blk_counts [nb, E], nb = ceil(T / kPermBlock)
+// (remap: optional logical expert -> physical slot map; counts then per slot)
 cudaError_t launch_block_counts(const int32_t* topk_idx, int T, int k, int E, int32_t* blk_counts,
-                                int32_t* status, cudaStream_t s);
+                                int32_t* status, cudaStream_t s, const int32_t* remap = nullptr);
 
 // counts [E] (nullable), offsets [E+1] (written, or read and checked if given),
 // blk_base [nb, E] = first row of each (block, expert)
@@ -34,7 +35,11 @@ cudaError_t launch_scan(const int32_t* blk_counts, int nb, int E, int R, int32_t
 // stable ranks: row_of_slot [T*k], slot_of_row [T*k]
 cudaError_t launch_rank(const int32_t* topk_idx, int T, int k, int E, const int32_t* blk_base,
                         int32_t* row_of_slot, int32_t* slot_of_row, int32_t* status,
-                        cudaStream_t s);
+                        cudaStream_t s, const int32_t* remap = nullptr);
+
+// out[e] (int64, zeroed here) = sum of q[t] over the (t, j) with topk_idx[t,j] = e
+cudaError_t launch_weighted_counts(const int32_t* topk_idx, const int32_t* q, int T, int k, int E,
+                                   int64_t* out, int32_t* status, cudaStream_t s);
 
 // T <= kPermBlock: counts, offsets, row_of_slot and slot_of_row in one launch
 cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, int32_t* counts,
@@ -48,7 +53,8 @@ cudaError_t launch_copy_rows(const void* x, const int32_t* row_of_slot, int T, i
 // packed weights: [E][2I][H] (gate/up interleaved in 128-row halves of 256-row
 // tiles) followed by [E][H][I] (down, transposed)
 cudaError_t launch_prepack(const void* w_gate, const void* w_up, const void* w_down, int E, int H,
-                           int I, void* packed, cudaStream_t s);
+                           int I, void* packed, cudaStream_t s,
+                           const int32_t* slot_of_expert = nullptr);
 
 // A bf16 row-major operand [rows, cols] of a grouped GEMM.  encode() writes a TMA
 // map of it with boxes of 64 columns x box_rows rows and 128-byte swizzle

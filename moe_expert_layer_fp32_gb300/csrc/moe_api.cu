@@ -153,21 +153,25 @@ namespace {
 
 // ------------------------------------------------------------ step bodies ---
 moe_status do_load_stats(const int32_t* idx, const moe_dims& d, int32_t* counts,
-                         int32_t* offsets, bool offsets_given, void* ws, cudaStream_t s) {
+                         int32_t* offsets, bool offsets_given, void* ws, cudaStream_t s,
+                         const int32_t* remap = nullptr) {
   const Layout L = layout(d);
   const int nb = (d.T + kPermBlock - 1) / kPermBlock;
   int32_t* status = at<int32_t>(ws, L.status);
-  MOE_CUDA(launch_block_counts(idx, d.T, d.k, d.E, at<int32_t>(ws, L.blk_counts), status, s));
+  MOE_CUDA(launch_block_counts(idx, d.T, d.k, d.E, at<int32_t>(ws, L.blk_counts), status, s,
+                               remap));
   MOE_CUDA(launch_scan(at<int32_t>(ws, L.blk_counts), nb, d.E, d.T * d.k, counts, offsets,
                        offsets_given, at<int32_t>(ws, L.blk_base), status, s));
   return MOE_OK;
 }
 
 moe_status do_permute_rows(const void* x, const int32_t* idx, const moe_dims& d, void* x_perm,
-                           int32_t* ros, int32_t* sor, void* ws, cudaStream_t s) {
+                           int32_t* ros, int32_t* sor, void* ws, cudaStream_t s,
+                           const int32_t* remap = nullptr) {
   const Layout L = layout(d);
   int32_t* status = at<int32_t>(ws, L.status);
-  MOE_CUDA(launch_rank(idx, d.T, d.k, d.E, at<int32_t>(ws, L.blk_base), ros, sor, status, s));
+  MOE_CUDA(launch_rank(idx, d.T, d.k, d.E, at<int32_t>(ws, L.blk_base), ros, sor, status, s,
+                       remap));
   MOE_CUDA(launch_copy_rows(x, ros, d.T, d.H, d.k, x_perm, status, s));
   return MOE_OK;
 }
@@ -342,6 +346,102 @@ moe_status moe_load_summary_host(const int32_t* counts_host, int32_t E, double* 
   return MOE_OK;
 }
 
+moe_status moe_load_stats_ex(const int32_t* topk_idx, const int32_t* slot_of_expert,
+                             const int32_t* q, moe_dims d, int32_t* counts, int32_t* offsets,
+                             int64_t* weighted_counts, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T > 0) MOE_TRY(need(topk_idx));
+  MOE_TRY(need(counts));
+  MOE_TRY(need(offsets));
+  if (slot_of_expert != nullptr) MOE_TRY(need(slot_of_expert));
+  if (weighted_counts != nullptr) {
+    MOE_TRY(need(weighted_counts));
+    if (q == nullptr) return MOE_ERR_INVALID_ARG;
+    if (d.T > 0) MOE_TRY(need(q));
+  }
+  MOE_TRY(check_ws(d, workspace, ws_bytes));
+  MOE_TRY(device_ok());
+  cudaStream_t s = as_stream(stream);
+  MOE_TRY(do_load_stats(topk_idx, d, counts, offsets, false, workspace, s, slot_of_expert));
+  if (weighted_counts != nullptr)
+    MOE_CUDA(launch_weighted_counts(topk_idx, q, d.T, d.k, d.E, weighted_counts,
+                                    at<int32_t>(workspace, layout(d).status), s));
+  return MOE_OK;
+}
+
+moe_status moe_lpt_placement_host(const int64_t* loads, int32_t E, int32_t P,
+                                  int32_t* slot_of_expert, int64_t* rank_loads) {
+  if (loads == nullptr || slot_of_expert == nullptr || E <= 0 || P <= 0 || E % P != 0 ||
+      E > kMaxE)
+    return MOE_ERR_INVALID_ARG;
+  const int Hs = E / P;
+  int64_t G[kMaxE] = {};
+  int n[kMaxE] = {};
+  int order[kMaxE];
+  for (int e = 0; e < E; ++e) order[e] = e;
+  // experts by (load descending, index ascending); insertion sort keeps it plain
+  for (int i = 1; i < E; ++i) {
+    const int v = order[i];
+    int j = i - 1;
+    while (j >= 0 && (loads[order[j]] < loads[v] || (loads[order[j]] == loads[v] && order[j] > v))) {
+      order[j + 1] = order[j];
+      --j;
+    }
+    order[j + 1] = v;
+  }
+  for (int i = 0; i < E; ++i) {
+    const int e = order[i];
+    int best = -1;
+    for (int p = 0; p < P; ++p)
+      if (n[p] < Hs && (best < 0 || G[p] < G[best])) best = p;  // ties: lower rank
+    slot_of_expert[e] = best * Hs + n[best];
+    G[best] += loads[e];
+    n[best] += 1;
+  }
+  if (rank_loads != nullptr)
+    for (int p = 0; p < P; ++p) rank_loads[p] = G[p];
+  return MOE_OK;
+}
+
+moe_status moe_rank_load_summary_host(const int64_t* rank_loads, int32_t P, double* cv,
+                                      double* eta_ep) {
+  if (rank_loads == nullptr || P <= 0) return MOE_ERR_INVALID_ARG;
+  double mean = 0.0, mx = 0.0;
+  for (int p = 0; p < P; ++p) {
+    mean += (double)rank_loads[p];
+    mx = fmax(mx, (double)rank_loads[p]);
+  }
+  mean /= P;
+  double var = 0.0;
+  for (int p = 0; p < P; ++p) var += ((double)rank_loads[p] - mean) * ((double)rank_loads[p] - mean);
+  var /= P;
+  if (cv) *cv = mean > 0 ? sqrt(var) / mean : 0.0;
+  if (eta_ep) *eta_ep = mx > 0 ? mean / mx : 1.0;
+  return MOE_OK;
+}
+
+moe_status moe_permute_ex(const void* x, const int32_t* topk_idx, const int32_t* slot_of_expert,
+                          const int32_t* offsets, moe_dims d, void* x_perm, int32_t* row_of_slot,
+                          int32_t* slot_of_row, void* workspace, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(d));
+  MOE_TRY(need(offsets));
+  MOE_TRY(check_ws(d, workspace, ws_bytes));
+  if (slot_of_expert != nullptr) MOE_TRY(need(slot_of_expert));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(need(x));
+  MOE_TRY(need(topk_idx));
+  MOE_TRY(need(x_perm));
+  MOE_TRY(need(row_of_slot));
+  MOE_TRY(need(slot_of_row));
+  MOE_TRY(device_ok());
+  cudaStream_t s = as_stream(stream);
+  MOE_TRY(do_load_stats(topk_idx, d, nullptr, const_cast<int32_t*>(offsets), true, workspace, s,
+                        slot_of_expert));
+  return do_permute_rows(x, topk_idx, d, x_perm, row_of_slot, slot_of_row, workspace, s,
+                         slot_of_expert);
+}
+
 moe_status moe_permute(const void* x, const int32_t* topk_idx, const int32_t* offsets, moe_dims d,
                        void* x_perm, int32_t* row_of_slot, int32_t* slot_of_row, void* workspace,
                        size_t ws_bytes, void* stream) {
@@ -358,6 +458,23 @@ moe_status moe_permute(const void* x, const int32_t* topk_idx, const int32_t* of
   cudaStream_t s = as_stream(stream);
   MOE_TRY(do_load_stats(topk_idx, d, nullptr, const_cast<int32_t*>(offsets), true, workspace, s));
   return do_permute_rows(x, topk_idx, d, x_perm, row_of_slot, slot_of_row, workspace, s);
+}
+
+moe_status moe_prepack_expert_weights_ex(const void* w_gate, const void* w_up,
+                                         const void* w_down, const int32_t* slot_of_expert,
+                                         moe_dims d, void* packed, size_t packed_bytes,
+                                         void* stream) {
+  MOE_TRY(check_dims(d));
+  MOE_TRY(need(w_gate));
+  MOE_TRY(need(w_up));
+  MOE_TRY(need(w_down));
+  MOE_TRY(need(packed));
+  if (slot_of_expert != nullptr) MOE_TRY(need(slot_of_expert));
+  if (packed_bytes < moe_packed_weight_bytes(d)) return MOE_ERR_WORKSPACE;
+  MOE_TRY(device_ok());
+  MOE_CUDA(launch_prepack(w_gate, w_up, w_down, d.E, d.H, d.I, packed, as_stream(stream),
+                          slot_of_expert));
+  return MOE_OK;
 }
 
 moe_status moe_prepack_expert_weights(const void* w_gate, const void* w_up, const void* w_down,

@@ -16,11 +16,17 @@ namespace {
 
 // src: per expert a [rows x cols] row-major matrix.  Writes dst[(e, map(col)), row].
 // mode 0: gate half of W1, mode 1: up half of W1, mode 2: W2.
+// slot_of_expert (optional): expert e is written to physical slot slot_of_expert[e]
+// (RoutePack's materialisation of a placement: each expert's weights move into the
+// tensors of its destination slot).
 __global__ void __launch_bounds__(256) transpose_pack_kernel(const uint16_t* __restrict__ src,
                                                              int rows, int cols, int mode, int I,
-                                                             int H, uint16_t* __restrict__ dst) {
+                                                             int H, uint16_t* __restrict__ dst,
+                                                             const int32_t* __restrict__ slot_of_expert) {
   __shared__ uint16_t tile[32][33];
   const int e = blockIdx.z;
+  const int de = slot_of_expert != nullptr ? __ldg(slot_of_expert + e) : e;
+  if (de < 0 || de >= (int)gridDim.z) return;  // a slot outside [0, E) is not written
   const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
   const uint16_t* s = src + (size_t)e * rows * cols;
   for (int i = threadIdx.y; i < 32; i += 8) {
@@ -35,10 +41,10 @@ __global__ void __launch_bounds__(256) transpose_pack_kernel(const uint16_t* __r
     size_t drow;
     int dld;
     if (mode < 2) {
-      drow = (size_t)e * 2 * I + (size_t)(c / 128) * 256 + (c % 128) + (mode == 1 ? 128 : 0);
+      drow = (size_t)de * 2 * I + (size_t)(c / 128) * 256 + (c % 128) + (mode == 1 ? 128 : 0);
       dld = H;
     } else {
-      drow = (size_t)e * H + c;
+      drow = (size_t)de * H + c;
       dld = I;
     }
     dst[drow * dld + r] = tile[threadIdx.x][i];
@@ -48,17 +54,18 @@ __global__ void __launch_bounds__(256) transpose_pack_kernel(const uint16_t* __r
 }  // namespace
 
 cudaError_t launch_prepack(const void* w_gate, const void* w_up, const void* w_down, int E, int H,
-                           int I, void* packed, cudaStream_t s) {
+                           int I, void* packed, cudaStream_t s, const int32_t* slot_of_expert) {
   uint16_t* w1 = static_cast<uint16_t*>(packed);
   uint16_t* w2 = w1 + (size_t)E * 2 * I * H;
   dim3 block(32, 8);
   dim3 g1((I + 31) / 32, (H + 31) / 32, E);  // gate/up: [H x I] per expert
   transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_gate), H, I, 0, I, H,
-                                             w1);
-  transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_up), H, I, 1, I, H, w1);
+                                             w1, slot_of_expert);
+  transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_up), H, I, 1, I, H, w1,
+                                             slot_of_expert);
   dim3 g2((H + 31) / 32, (I + 31) / 32, E);  // down: [I x H] per expert
   transpose_pack_kernel<<<g2, block, 0, s>>>(static_cast<const uint16_t*>(w_down), I, H, 2, I, H,
-                                             w2);
+                                             w2, slot_of_expert);
   return cudaGetLastError();
 }
 

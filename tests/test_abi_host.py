@@ -100,3 +100,21 @@ def test_load_summary_host(moe):
 def test_status_strings(moe):
     for code in range(8):
         assert moe._lib.moe_status_string(code)
+
+
+def test_lpt_placement_host_matches_oracle(moe):
+    """The library's host LPT planner and rank metrics equal the oracle's."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(5)
+    for E, P in [(8, 2), (64, 8), (256, 16), (128, 4)]:
+        loads = (rng.zipf(1.4, E) * 37 + rng.integers(0, 9, E)).astype(np.int64)
+        loads[: E // 4] = loads[E // 4: E // 2]  # equal loads exercise the tie rules
+        pi, G = moe.moe_lpt_placement_host(loads, P)
+        pi_o, G_o = oracle.lpt_placement(loads, P)
+        np.testing.assert_array_equal(pi, pi_o)
+        np.testing.assert_array_equal(G, G_o)
+        assert moe.moe_rank_load_summary_host(G) == pytest.approx(oracle.rank_metrics(G),
+                                                                   rel=1e-12)
+    with pytest.raises(moe.MoEError):
+        moe.moe_lpt_placement_host(np.ones(10, np.int64), 3)  # E not a multiple of P
