@@ -63,6 +63,14 @@ def _L():
         for f in ("oracle_weighted_counts", "oracle_lpt_placement", "oracle_rank_metrics",
                   "oracle_permute_remap"):
             getattr(lib, f).restype = ctypes.c_int
+        lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_tree_reduce.argtypes = [vp, i32, ctypes.c_int64, vp]
+        lib.oracle_combine_sharded.argtypes = [vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, i32,
+                                               i32, i32, i32, vp, vp, i32]
+        lib.oracle_shared_expert.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32]
+        for f in ("oracle_tree_reduce", "oracle_combine_sharded", "oracle_shared_expert"):
+            getattr(lib, f).restype = ctypes.c_int
         lib.oracle_exp_cw.argtypes = [ctypes.c_float]
         lib.oracle_exp_cw.restype = ctypes.c_float
         for f in ("oracle_router_logits", "oracle_route", "oracle_load_stats", "oracle_permute",
@@ -177,6 +185,53 @@ def permute_remap(x, idx, slot_of_expert, offsets, E, with_x_perm=True):
     _check(_L().oracle_permute_remap(_p(x), _p(idx), _p(pi), _p(offsets), T, H, E, k, _p(x_perm),
                                      _p(ros), _p(sor)), "permute_remap")
     return x_perm, ros, sor
+
+
+def f64_to_bf16(x: float) -> int:
+    """bf16 bits of x rounded once, to nearest even, straight from FP64."""
+    return int(_L().oracle_f64_to_bf16(float(x)))
+
+
+def tree_reduce(partials):
+    """out [N] bf16 bits: the fixed FP64 pairwise tree over partials [G, ...] (bf16 bits)."""
+    p = _c(partials, np.uint16)
+    G = p.shape[0]
+    flat = p.reshape(G, -1)
+    out = np.empty(flat.shape[1], dtype=np.uint16)
+    _check(_L().oracle_tree_reduce(_p(flat), G, flat.shape[1], _p(out)), "tree_reduce")
+    return out.reshape(p.shape[1:])
+
+
+def combine_sharded(y, w, idx, row_of_slot, owner, G, scale=1.0, shared=None, want_partials=False,
+                    nthreads=0):
+    """out [T, H] bf16 bits (and partials [G, T, H] if want_partials): per-rank
+    slot-order chains over the experts each rank owns, FP64 tree across ranks."""
+    y = _c(y, np.float32)
+    w = _c(w, np.float32)
+    idx = _c(idx, np.int32)
+    ros = _c(row_of_slot, np.int32).reshape(-1)
+    owner = _c(owner, np.int32)
+    T, k = w.shape
+    H = y.shape[1]
+    sh = None if shared is None else _c(shared, np.float32)
+    out = np.empty((T, H), dtype=np.uint16)
+    parts = np.empty((G, T, H), dtype=np.uint16) if want_partials else None
+    _check(_L().oracle_combine_sharded(_p(y), _p(w), _p(idx), _p(ros), _p(owner), int(G),
+                                       float(scale), _p(sh), T, H, owner.shape[0], k, _p(parts),
+                                       _p(out), nthreads), "combine_sharded")
+    return (out, parts) if want_partials else out
+
+
+def shared_expert(x, wg, wu, wd, G, nthreads=0):
+    """shared [G, T, H] FP32: the shared expert's G intermediate-column shards."""
+    x = _c(x, np.uint16)
+    wg, wu, wd = _c(wg, np.uint16), _c(wu, np.uint16), _c(wd, np.uint16)
+    T, H = x.shape
+    Is = wg.shape[1]
+    out = np.empty((G, T, H), dtype=np.float32)
+    _check(_L().oracle_shared_expert(_p(x), _p(wg), _p(wu), _p(wd), T, H, Is, int(G), _p(out),
+                                     nthreads), "shared_expert")
+    return out
 
 
 def exp_cw(x: float) -> float:

@@ -24,6 +24,13 @@
 //  * "HARTS", section 3.4 "MoE semantics without expert expansion":
 //    deterministic, no-token-drop top-k routing; Eq. 23 imbalance max/mean - 1.
 //  * RoutePack, section 6 Eq. 22: coefficient of variation of loads.
+//  * "0 train-infer mismatch for open-weight MoE RL", section "Sharding the
+//    experts": each expert rank ends with one BF16 partial per token (slots it
+//    does not own add exact zeros; its shared-expert shard is added before the
+//    rounding); the partials are summed in a fixed logical order by adjacent
+//    pairs in FP64, an odd last one carried up a level unchanged, one BF16
+//    rounding at the end.  Section "Mixture-of-experts layers" (shared expert):
+//    the fixed-K projections and SwiGLU of the dense case.
 //
 // Readings where the pages leave a step open (each stated again where used):
 //  R1 router dot product: FP32 fused multiply-add chain over ascending h from 0,
@@ -36,6 +43,14 @@
 //  R6 expert GEMMs: FP32 accumulation over ascending K; only h = SwiGLU output is
 //     rounded to BF16; y stays FP32;
 //  R7 combine: FMA chain over slots j = 0..k-1 from 0, one BF16 round.
+//  R8 sharded combine: rank g's partial is the same chain with y replaced by an
+//     exact 0.0f in the slots whose expert another rank owns, then one FP32 add
+//     of g's shared-expert shard output (if any), then one BF16 round;
+//  R9 the FP64 tree's final rounding goes straight from FP64 to BF16 (round to
+//     nearest, ties to even), not through FP32;
+//  R10 shared expert sharded G ways: rank g holds intermediate columns
+//     [g*Is/G, (g+1)*Is/G) of the gate/up projections and the same rows of the
+//     down projection, and computes them as one expert over all tokens.
 //
 // Build: g++ -O2 -std=c++17 -ffp-contract=off (no contraction: every a*b+c below
 // rounds twice unless written as std::fma).
@@ -65,6 +80,48 @@ inline uint16_t f32_to_bf16(float f) {
   uint32_t lsb = (u >> 16) & 1u;
   u += 0x7FFFu + lsb;
   return (uint16_t)(u >> 16);
+}
+
+// f64 -> bf16 in one rounding (reading R9).  Definition: of the two bf16 values
+// next to |x| at the bf16 spacing of its binade, the nearer; on a tie the one
+// whose last mantissa bit is even; beyond the largest finite bf16 (after
+// rounding) infinity.  NaN -> 0x7FC0.
+inline uint16_t f64_to_bf16(double x) {
+  if (std::isnan(x)) return 0x7FC0;
+  const uint16_t sign = std::signbit(x) ? 0x8000 : 0;
+  const double a = std::fabs(x);
+  if (std::isinf(a)) return sign | 0x7F80;
+  if (a == 0.0) return sign;
+  int ex;
+  std::frexp(a, &ex);                           // a in [2^(ex-1), 2^ex)
+  const int e = std::max(ex - 1, -126);         // bf16 subnormals share 2^-126's spacing
+  const double ulp = std::ldexp(1.0, e - 7);    // 7 stored mantissa bits
+  const double n = std::floor(a / ulp);         // exact: ulp is a power of two
+  const double lo = n * ulp, hi = lo + ulp;     // both exact
+  const double dlo = a - lo, dhi = hi - a;      // both exact (Sterbenz, or lo = 0)
+  double r;
+  if (dlo < dhi) r = lo;
+  else if (dhi < dlo) r = hi;
+  else r = (std::fmod(n, 2.0) == 0.0) ? lo : hi;
+  if (r >= std::ldexp(1.0, 128)) return sign | 0x7F80;
+  const float f = (float)r;  // exact: r is a bf16 value
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  return sign | (uint16_t)(u >> 16);
+}
+
+// The fixed expert-output reduction: v holds the contributors in logical order,
+// widened to FP64.  Each level adds adjacent pairs in FP64 and carries an odd
+// last value unchanged, until one value remains.
+double fp64_pairwise_tree(std::vector<double>& v) {
+  size_t n = v.size();
+  while (n > 1) {
+    size_t m = 0;
+    for (size_t i = 0; i + 1 < n; i += 2) v[m++] = v[i] + v[i + 1];
+    if (n & 1) v[m++] = v[n - 1];
+    n = m;
+  }
+  return n == 1 ? v[0] : 0.0;
 }
 
 // Run body(i) for i in [0, n) on up to nthreads threads (contiguous chunks).
@@ -454,6 +511,80 @@ int oracle_combine_scaled(const float* y, const float* w, const int32_t* row_of_
       out[t * H + c] = f32_to_bf16(acc);
     }
   });
+  return 0;
+}
+
+uint16_t oracle_f64_to_bf16(double x) { return f64_to_bf16(x); }
+
+// Fixed expert-output reduction of G BF16 partials: partials [G][N] (logical
+// order g = 0..G-1), out [N] = bf16(tree(partials[.][n])) (reading R9).
+int oracle_tree_reduce(const uint16_t* partials, int G, int64_t N, uint16_t* out) {
+  if (G < 1 || N < 0) return 1;
+  std::vector<double> v(G);
+  for (int64_t n = 0; n < N; ++n) {
+    for (int g = 0; g < G; ++g) v[g] = (double)bf16_to_f32(partials[(int64_t)g * N + n]);
+    out[n] = f64_to_bf16(fp64_pairwise_tree(v));
+  }
+  return 0;
+}
+
+// Sharded combine (reading R8): owner[e] in [0, G) is the rank that owns logical
+// expert e.  For every token t, column c and rank g:
+//   acc = 0; for j = 0..k-1: acc = fma(scale * w[t,j], owner[idx[t,j]] == g ? y[row,c] : 0, acc)
+//   if shared (shared [G][T][H] FP32): acc = acc + shared[g,t,c]
+//   partial[g,t,c] = bf16(acc)
+// out[t,c] = bf16(FP64 tree over partial[0..G-1,t,c]).  partials_out is optional.
+int oracle_combine_sharded(const float* y, const float* w, const int32_t* idx,
+                           const int32_t* row_of_slot, const int32_t* owner, int G, float scale,
+                           const float* shared, int T, int H, int E, int k, uint16_t* partials_out,
+                           uint16_t* out, int nthreads) {
+  if (T < 0 || H <= 0 || E <= 0 || k < 1 || G < 1) return 1;
+  for (int e = 0; e < E; ++e)
+    if (owner[e] < 0 || owner[e] >= G) return 1;
+  parallel_for(T, nthreads, [&](int64_t t) {
+    std::vector<double> v(G);
+    for (int c = 0; c < H; ++c) {
+      for (int g = 0; g < G; ++g) {
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j) {
+          const int e = idx[t * k + j];
+          const int64_t r = row_of_slot[t * k + j];
+          const float val = (owner[e] == g) ? y[r * H + c] : 0.0f;
+          acc = std::fma(scale * w[t * k + j], val, acc);
+        }
+        if (shared) acc = acc + shared[((int64_t)g * T + t) * H + c];
+        const uint16_t p = f32_to_bf16(acc);
+        if (partials_out) partials_out[((int64_t)g * T + t) * H + c] = p;
+        v[g] = (double)bf16_to_f32(p);
+      }
+      out[t * H + c] = f64_to_bf16(fp64_pairwise_tree(v));
+    }
+  });
+  return 0;
+}
+
+// Shared expert sharded G ways (reading R10): W_gate, W_up [H, Is], W_down [Is, H]
+// (bf16 bits, row-major).  Rank g takes intermediate columns [g*Is/G, (g+1)*Is/G)
+// and runs them as one expert over all T tokens (oracle_expert_ffn with E = 1).
+// shared [G][T][H] FP32.
+int oracle_shared_expert(const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
+                         const uint16_t* wd, int T, int H, int Is, int G, float* shared,
+                         int nthreads) {
+  if (T < 0 || H <= 0 || Is <= 0 || G < 1 || Is % G != 0) return 1;
+  const int Ig = Is / G;
+  std::vector<uint16_t> sg((size_t)H * Ig), su((size_t)H * Ig);
+  const int32_t offsets[2] = {0, T};
+  for (int g = 0; g < G; ++g) {
+    for (int h = 0; h < H; ++h)
+      for (int i = 0; i < Ig; ++i) {
+        sg[(size_t)h * Ig + i] = wg[(size_t)h * Is + (size_t)g * Ig + i];
+        su[(size_t)h * Ig + i] = wu[(size_t)h * Is + (size_t)g * Ig + i];
+      }
+    const uint16_t* sd = wd + (size_t)g * Ig * H;  // rows g*Ig .. (g+1)*Ig - 1
+    const int rc = oracle_expert_ffn(x, offsets, sg.data(), su.data(), sd, 1, H, Ig, nullptr,
+                                     shared + (size_t)g * T * H, nthreads);
+    if (rc) return rc;
+  }
   return 0;
 }
 

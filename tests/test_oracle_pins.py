@@ -555,3 +555,201 @@ def test_permute_remap_groups_by_physical_slot():
         e = int(np.flatnonzero(pi == slot)[0])
         assert np.all(np.diff(toks) > 0) and np.all((idx[toks] == e).any(axis=1))
     np.testing.assert_array_equal(xp, x[sor // k])
+
+
+# ------------------------------------------- sharded experts: FP64 tree ---
+from fractions import Fraction  # noqa: E402
+
+
+def bf16_value(bits):
+    """Exact value of bf16 bits as a Fraction (finite values only)."""
+    bits = int(bits)
+    sign = -1 if bits & 0x8000 else 1
+    ex = (bits >> 7) & 0xFF
+    man = bits & 0x7F
+    assert ex != 0xFF
+    if ex == 0:
+        return sign * Fraction(man) * Fraction(2) ** -133
+    return sign * (Fraction(128 + man) * Fraction(2) ** (ex - 134))
+
+
+def is_nearest_even_bf16(q, bits):
+    """bits is the round-to-nearest-even bf16 of the exact value q: no finite bf16
+    neighbour is nearer, and on a tie the kept mantissa is even."""
+    bits = int(bits)
+    if (bits & 0x7FFF) == 0x7F80:  # infinity: q at or beyond max + half a spacing
+        return abs(q) >= bf16_value(0x7F7F) + Fraction(2) ** (127 - 8)
+    v = bf16_value(bits)
+    if v != 0 and (v > 0) != (q > 0):
+        return False
+    mag = bits & 0x7FFF
+    s = bits & 0x8000
+    d = abs(q - v)
+    for nb in (mag - 1, mag + 1):
+        if nb < 0:
+            continue
+        if nb >= 0x7F80:
+            continue
+        dn = abs(q - bf16_value(s | nb))
+        if dn < d:
+            return False
+        if dn == d and (mag & 1):
+            return False
+    if mag == 0 and q != 0:  # rounded to zero: the zero keeps the sign of q
+        return (q < 0) == bool(s)
+    return True
+
+
+def test_f64_to_bf16_is_round_to_nearest_even():
+    """Catches double rounding through FP32, truncation, a wrong tie rule, a
+    wrong subnormal spacing and a missed overflow: each result is checked against
+    its exact neighbours."""
+    rng = np.random.default_rng(11)
+    xs = [1 + 2 ** -8 + 2 ** -40, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8 + 2 ** -60),
+          2 ** -134, 3 * 2 ** -135, 2 ** -133 * 1.5, 2 ** -140, 2 ** -127 * 1.75,
+          3.3895313892515355e38, 3.39e38, 3.4e38, -1e300, 1e-300, 0.0, -0.0]
+    xs += list(rng.standard_normal(2000) * 10.0 ** rng.integers(-40, 38, 2000))
+    # values at and near every kind of bf16 tie
+    for b in rng.integers(0x0001, 0x7F7F, 500):
+        lo, hi = bf16_value(int(b)), bf16_value(int(b) + 1)
+        mid = (lo + hi) / 2
+        xs += [float(mid), float(mid) * (1 + 2 ** -45), float(mid) * (1 - 2 ** -45)]
+    for x in xs:
+        bits = oracle.f64_to_bf16(x)
+        if x == 0.0:
+            assert bits == (0x8000 if math.copysign(1, x) < 0 else 0)
+            continue
+        assert is_nearest_even_bf16(Fraction(x), bits), (x, hex(bits))
+        assert (bits >> 15) == (1 if x < 0 else 0)
+
+
+def test_f64_to_bf16_equals_library_rounding_on_f32_values():
+    """Values that FP32 holds exactly: one rounding from FP64 equals torch's
+    float32 -> bfloat16 (round to nearest even)."""
+    import torch
+    f = synth.normal_f32(5, synth.TID_MISC, (4000,), 3.0)
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.f64_to_bf16(float(v)) for v in f], np.uint16)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_fp64_tree_golden():
+    """Hand-derived cases: pairs vs left-to-right, the odd carry at 3 and 5
+    contributors, FP64 vs FP32 accumulation, one final rounding, signed zeros."""
+    fx = load("fp64_tree.json")
+    for c in fx["cases"]:
+        p = np.array(c["partials_bf16_bits"], np.uint16).reshape(-1, 1)
+        assert int(oracle.tree_reduce(p)[0]) == c["expected_bf16_bits"], c["name"]
+
+
+def test_fp64_tree_is_rounded_exact_sum_when_fp64_holds_every_node():
+    """Partials within a 2^20 range: every FP64 partial sum is exact, so the
+    tree's result is the exact sum rounded once.  Catches a dropped contributor,
+    a wrong carry, FP32 accumulation and a second rounding, for G = 1..16."""
+    rng = np.random.default_rng(12)
+    for G in range(1, 17):
+        vals = rng.standard_normal((G, 300)) * 2.0 ** rng.integers(-10, 10, (G, 300))
+        p = f32_to_bf16_bits(vals.astype(np.float32))
+        out = oracle.tree_reduce(p)
+        for n in range(p.shape[1]):
+            q = sum(bf16_value(b) for b in p[:, n])
+            assert is_nearest_even_bf16(q, out[n]) or (q == 0 and out[n] in (0, 0x8000)), (G, n)
+
+
+def test_sharded_combine_golden():
+    fx = load("sharded_combine.json")
+    for c in fx["cases"]:
+        sh = None if c["shared"] is None else np.array(c["shared"], np.float32)
+        out, parts = oracle.combine_sharded(np.array(c["y"], np.float32),
+                                            np.array(c["w"], np.float32),
+                                            np.array(c["idx"], np.int32),
+                                            np.array(c["row_of_slot"], np.int32),
+                                            np.array(c["owner"], np.int32), c["G"], 1.0, sh,
+                                            want_partials=True)
+        np.testing.assert_array_equal(parts, np.array(c["expected_partials_bf16_bits"]),
+                                      err_msg=c["name"])
+        np.testing.assert_array_equal(out, np.array(c["expected_out_bf16_bits"]),
+                                      err_msg=c["name"])
+
+
+def _sharded_case(T=40, H=24, E=12, k=4, seed=13):
+    rng = np.random.default_rng(seed)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    ros = rng.permutation(T * k).astype(np.int32).reshape(T, k)
+    y = synth.normal_f32(seed, synth.TID_Y, (T * k, H), 1.0)
+    w = synth.uniform_f32(seed, synth.TID_TOPK_W, (T, k), 0.0, 1.0)
+    return idx, ros, y, w
+
+
+def test_sharded_combine_one_rank_is_the_combine():
+    """G = 1 (or every expert on rank 0 of G = 4, the other partials +0): the
+    output is the pinned slot-order combine, bit for bit."""
+    idx, ros, y, w = _sharded_case()
+    E = 12
+    ref = oracle.combine_scaled(y, w, ros, 2.5)
+    for G in (1, 4):
+        out = oracle.combine_sharded(y, w, idx, ros, np.zeros(E, np.int32), G, 2.5)
+        np.testing.assert_array_equal(out, ref)
+
+
+def test_sharded_partials_are_combines_of_owned_rows():
+    """Rank g's partial equals the plain combine of y with every row whose expert
+    another rank owns replaced by zeros.  Catches owner looked up by slot instead
+    of by expert, and a partial that skips the rounding."""
+    idx, ros, y, w = _sharded_case()
+    E, G, T, k = 12, 3, 40, 4
+    owner = (np.arange(E) * 7 % G).astype(np.int32)
+    out, parts = oracle.combine_sharded(y, w, idx, ros, owner, G, 1.0, want_partials=True)
+    for g in range(G):
+        yg = y.copy()
+        for t in range(T):
+            for j in range(k):
+                if owner[idx[t, j]] != g:
+                    yg[ros[t, j]] = 0.0
+        np.testing.assert_array_equal(parts[g], oracle.combine(yg, w, ros))
+    np.testing.assert_array_equal(out, oracle.tree_reduce(parts))
+
+
+def test_sharded_combine_close_to_float64_sum():
+    idx, ros, y, w = _sharded_case(T=64, H=32, E=16, k=6, seed=14)
+    owner = (np.arange(16) // 4).astype(np.int32)
+    sh = synth.normal_f32(15, synth.TID_MISC, (4, 64, 32), 0.5)
+    out = f32(oracle.combine_sharded(y, w, idx, ros, owner, 4, 1.0, sh))
+    ref = np.einsum("tj,tjc->tc", w.astype(np.float64), y[ros].astype(np.float64)) + sh.sum(0)
+    bound = 2.0 ** -8 * (np.abs(y[ros]).max() * w.sum(1, keepdims=True) * 1.0 + np.abs(sh).sum(0)) \
+        + 2.0 ** -8 * np.abs(ref)
+    assert np.all(np.abs(out - ref) <= bound)
+
+
+def _swiglu_f64(x, wg, wu, wd):
+    g = x @ wg
+    u = x @ wu
+    h = f32(f32_to_bf16_bits((silu64(g) * u).astype(np.float32)))
+    return h.astype(np.float64) @ wd
+
+
+def test_shared_expert_shards():
+    """Shard g uses intermediate columns [g*Is/G, (g+1)*Is/G) only (changing
+    another shard's columns leaves it unchanged), each shard is the dense SwiGLU
+    FFN of its slice, and the shards add up to the dense FFN over all of Is."""
+    T, H, Is, G = 20, 32, 48, 4
+    x = synth.normal_bf16(16, synth.TID_X, (T, H), 1.0)
+    wg = synth.normal_bf16(16, synth.TID_WG, (H, Is), 0.2)
+    wu = synth.normal_bf16(16, synth.TID_WU, (H, Is), 0.2)
+    wd = synth.normal_bf16(16, synth.TID_WD, (Is, H), 0.2)
+    ys = oracle.shared_expert(x, wg, wu, wd, G)
+    X = f32(x).astype(np.float64)
+    Wg, Wu, Wd = (f32(a).astype(np.float64) for a in (wg, wu, wd))
+    Ig = Is // G
+    for g in range(G):
+        sl = slice(g * Ig, (g + 1) * Ig)
+        ref = _swiglu_f64(X, Wg[:, sl], Wu[:, sl], Wd[sl])
+        np.testing.assert_allclose(ys[g], ref, rtol=0, atol=2e-3 * np.abs(ref).max() + 1e-6)
+    dense = _swiglu_f64(X, Wg, Wu, Wd)
+    np.testing.assert_allclose(ys.astype(np.float64).sum(0), dense, rtol=0,
+                               atol=2e-3 * np.abs(dense).max() + 1e-6)
+    wg2 = wg.copy()
+    wg2[:, Ig:2 * Ig] ^= 0x0040  # change shard 1's gate columns
+    ys2 = oracle.shared_expert(x, wg2, wu, wd, G)
+    np.testing.assert_array_equal(ys2[[0, 2, 3]], ys[[0, 2, 3]])
+    assert not np.array_equal(ys2[1], ys[1])
