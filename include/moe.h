@@ -239,6 +239,33 @@ moe_status moe_combine(const float* y, const float* topk_w, const int32_t* row_o
 moe_status moe_combine_ex(const float* y, const float* topk_w, const int32_t* row_of_slot,
                           float route_scale, moe_dims d, void* out, void* stream);
 
+/* Combine as G expert ranks would do it, without the exchange ("0 train-infer
+ * mismatch for open-weight MoE RL", section "Sharding the experts").  owner [E]
+ * int32 (device) gives the rank in [0, G) that owns each logical expert; a slot
+ * whose expert has an owner outside [0, G) contributes to no rank.  For token t,
+ * column c and rank g = 0..G-1:
+ *   acc = 0; for j = 0..k-1:
+ *     acc = fmaf(route_scale * topk_w[t,j], owner[topk_idx[t,j]] == g ? y[row, c] : 0.0f, acc)
+ *   acc = acc + shared[g, t, c]          (if shared != NULL: [G, T, H] fp32, e.g.
+ *                                         from moe_shared_expert)
+ *   partial[g, t, c] = bf16(acc)         (round to nearest even)
+ * out[t, c] = bf16 of the FP64 pairwise tree over partial[0..G-1, t, c] (below).
+ *   partials [G, T, H] bf16 is optional (NULL: kept in registers only).
+ *   1 <= G <= 16; route_scale > 0 and finite.  Other arguments as moe_combine. */
+moe_status moe_combine_sharded(const float* y, const float* topk_w, const int32_t* topk_idx,
+                               const int32_t* row_of_slot, const int32_t* owner, int32_t G,
+                               float route_scale, const float* shared, moe_dims d, void* partials,
+                               void* out, void* stream);
+
+/* The fixed expert-output reduction (same section): for every n in [0, N),
+ * v = partials[0..G-1][n] (bf16, logical rank order) widened exactly to FP64;
+ * each level adds adjacent pairs (v0+v1, v2+v3, ...) in FP64 and carries an odd
+ * last value unchanged; the last value is rounded once, FP64 -> bf16, to nearest
+ * even.  partials [G][N] and out [N] bf16 on the device, 2-byte aligned
+ * (16-byte alignment and N % 8 == 0 take the vector path); 1 <= G <= 16. */
+moe_status moe_tree_reduce_bf16(const void* partials, int32_t G, int64_t N, void* out,
+                                void* stream);
+
 /* The whole layer forward: route -> load stats -> permute -> expert FFN ->
  * combine, enqueued on one stream with no host synchronisation.
  *   x [T, H] bf16; w_router [H, E] fp32; bias [E] fp32 or NULL; packed_weights

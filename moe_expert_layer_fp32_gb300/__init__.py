@@ -35,7 +35,8 @@ ABI_SYMBOLS = ("moe_workspace_bytes", "moe_packed_weight_bytes", "moe_route", "m
                "moe_read_device_status", "moe_status_string", "moe_load_stats_noalloc",
                "moe_set_wait_limit", "moe_route_ex", "moe_combine_ex", "moe_layer_fwd_ex",
                "moe_load_stats_ex", "moe_lpt_placement_host", "moe_rank_load_summary_host",
-               "moe_permute_ex", "moe_prepack_expert_weights_ex")
+               "moe_permute_ex", "moe_prepack_expert_weights_ex", "moe_combine_sharded",
+               "moe_tree_reduce_bf16")
 
 
 class moe_dims(ctypes.Structure):
@@ -96,6 +97,9 @@ _sig = {
                                       _vp]),
     "moe_prepack_expert_weights_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, moe_dims, _vp, _sz,
                                                      _vp]),
+    "moe_combine_sharded": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, ctypes.c_float, _vp,
+                                           moe_dims, _vp, _vp, _vp]),
+    "moe_tree_reduce_bf16": (ctypes.c_int, [_vp, _i32, ctypes.c_int64, _vp, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -225,6 +229,21 @@ def moe_prepack_expert_weights_ex(w_gate, w_up, w_down, slot_of_expert, d, packe
     _check("moe_prepack_expert_weights_ex", _lib.moe_prepack_expert_weights_ex(
         _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(slot_of_expert), d, _ptr(packed), nbytes,
         _stream(stream)))
+
+
+def moe_combine_sharded(y, topk_w, topk_idx, row_of_slot, owner, G, route_scale, shared, d, out,
+                        partials=None, stream=None):
+    """Per-rank BF16 partials (slots of other ranks as exact zeros, optional
+    shared-expert shards [G, T, H] fp32) reduced by the fixed FP64 pairwise tree."""
+    _check("moe_combine_sharded", _lib.moe_combine_sharded(
+        _ptr(y), _ptr(topk_w), _ptr(topk_idx), _ptr(row_of_slot), _ptr(owner), int(G),
+        float(route_scale), _ptr(shared), d, _ptr(partials), _ptr(out), _stream(stream)))
+
+
+def moe_tree_reduce_bf16(partials, G, N, out, stream=None):
+    """out [N] = bf16(FP64 pairwise tree over partials [G, N]) (bf16 tensors)."""
+    _check("moe_tree_reduce_bf16", _lib.moe_tree_reduce_bf16(_ptr(partials), int(G), int(N),
+                                                             _ptr(out), _stream(stream)))
 
 
 def moe_load_summary_host(counts_host):

@@ -10,6 +10,7 @@ namespace moe {
 
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
+constexpr int kMaxShards = 16;  // expert ranks of the sharded combine / tree
 constexpr int kPermBlock = 256;  // tokens per ranking block of the permutation
 constexpr long long kSpinLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int kRouteSmallMaxT = 64;  // batches up to this size use the small-T router kernel
@@ -82,6 +83,19 @@ int gemm_down_bn(int H);
 // out[t] = bf16(slot-order FMA chain of (scale * topk_w[t,j]) * y[row_of_slot[t*k+j]])
 cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, int T,
                            int H, int k, float scale, void* out, cudaStream_t s);
+
+// Sharded combine: G per-rank BF16 partials (slot-order FP32 chains, other ranks'
+// slots as exact zeros, optional shared [G][T][H] FP32 added before the rounding)
+// reduced by the fixed FP64 pairwise tree.  partials [G][T][H] bf16 is optional.
+cudaError_t launch_combine_sharded(const float* y, const float* topk_w, const int32_t* topk_idx,
+                                   const int32_t* row_of_slot, const int32_t* owner, int G, int T,
+                                   int H, int E, int k, float scale, const float* shared,
+                                   void* partials, void* out, cudaStream_t s);
+
+// out[n] = bf16(FP64 pairwise tree over partials[0..G-1][n]); vec: 16-byte vectors
+// (N a multiple of 8, all rows 16-byte aligned).
+cudaError_t launch_tree_reduce(const void* partials, int G, long long N, void* out, bool vec,
+                               cudaStream_t s);
 
 // number of SMs of the current device (cached per device)
 int device_sm_count();

@@ -524,6 +524,42 @@ moe_status moe_combine(const float* y, const float* topk_w, const int32_t* row_o
   return moe_combine_ex(y, topk_w, row_of_slot, 1.0f, d, out, stream);
 }
 
+moe_status moe_combine_sharded(const float* y, const float* topk_w, const int32_t* topk_idx,
+                               const int32_t* row_of_slot, const int32_t* owner, int32_t G,
+                               float route_scale, const float* shared, moe_dims d, void* partials,
+                               void* out, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (G < 1 || G > kMaxShards) return MOE_ERR_UNSUPPORTED;
+  if (!(route_scale > 0.0f) || !isfinite(route_scale)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(need(owner));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(need(y));
+  MOE_TRY(need(topk_w));
+  MOE_TRY(need(topk_idx));
+  MOE_TRY(need(row_of_slot));
+  MOE_TRY(need(out));
+  if (shared != nullptr) MOE_TRY(need(shared));
+  if (partials != nullptr) MOE_TRY(need(partials));
+  MOE_TRY(device_ok());
+  MOE_CUDA(launch_combine_sharded(y, topk_w, topk_idx, row_of_slot, owner, G, d.T, d.H, d.E, d.k,
+                                  route_scale, shared, partials, out, as_stream(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_tree_reduce_bf16(const void* partials, int32_t G, int64_t N, void* out,
+                                void* stream) {
+  if (G < 1 || N < 0) return MOE_ERR_INVALID_ARG;
+  if (G > kMaxShards) return MOE_ERR_UNSUPPORTED;
+  if (N == 0) return MOE_OK;
+  if (partials == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(partials) & 1) || (reinterpret_cast<uintptr_t>(out) & 1))
+    return MOE_ERR_MISALIGNED;
+  MOE_TRY(device_ok());
+  const bool vec = (N % 8 == 0) && aligned16(partials) && aligned16(out);
+  MOE_CUDA(launch_tree_reduce(partials, G, (long long)N, out, vec, as_stream(stream)));
+  return MOE_OK;
+}
+
 moe_status moe_layer_fwd(const void* x, const float* w_router, const float* bias,
                          const void* packed_weights, moe_dims d, void* out, int32_t* topk_idx_out,
                          float* topk_w_out, int32_t* counts_out, void* workspace, size_t ws_bytes,
