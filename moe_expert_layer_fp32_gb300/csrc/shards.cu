@@ -9,38 +9,40 @@
 // to the next level unchanged, with one BF16 rounding at the end.
 //
 // combine_sharded_kernel runs all G ranks of one token in one CTA: the k gathered
-// FP32 rows are read once, the G chains, the G roundings and the tree all stay in
+// FP32 rows are read once, the chains, the G roundings and the reduction stay in
 // registers, and only the final BF16 row (plus the partials, when asked for) is
 // written.  tree_reduce_kernel is the reduction alone, for partials that another
-// engine delivered: G BF16 rows in, one BF16 row out, 16-byte vectors.
+// engine delivered: G BF16 rows in, one BF16 row out.
 //
-// Format conversions are integer bit manipulation: bf16 -> f64 widens exactly, and
-// f64 -> bf16 rounds once to nearest even from the full 52-bit fraction, so no
-// value passes through FP32 on its way out (that would round twice).
-//
-// FP64 is a narrow pipe on this GPU, so the tree runs in FP32 wherever that is
-// provably the same.  Every leaf is a bf16 value (8 significant bits).  A group of
-// leaves whose exponents lie within W = 16 - ceil(log2 G) binades of each other
-// sums exactly in FP32 (the sum of their magnitudes stays below 2^24 units of the
-// smallest one), in any order.  The leaves are split at W binades below the
-// largest exponent into two such groups, H and L; if the smallest non-zero leaf is
-// within 2W + 1 binades of the largest, both sums are exact and H + L is the exact
-// sum of all leaves.  So is the FP64 tree's result: every node of it is a partial
-// sum of fewer than 2^53 units, hence exact.  H + L is rounded once to bf16:
-// s = fl(H + L) plus its exact TwoSum error decides the one case where s alone
-// cannot, a tie.  Both accumulators start at -0, so an all -0 input gives -0 and
-// any exact zero sum of other leaves +0, as IEEE addition in the tree gives it.
-// Wider spreads, leaves from 2^124 up (no FP32 overflow), infinities and NaNs take
-// the FP64 tree itself.
+// FP64 is a narrow pipe on this GPU, so the reduction runs in FP32 wherever that
+// is provably the same.  Every leaf is a bf16 value (8 significant bits).  A group
+// of at most G leaves whose exponents lie within W = 16 - ceil(log2 G) binades of
+// each other sums exactly in FP32 (the sum of their magnitudes stays below 2^24
+// units of the smallest one), in any order.  The leaves are split at W binades
+// below the largest exponent into two such groups, H and L; if the smallest
+// non-zero leaf is within 2W + 1 binades of the largest, both sums are exact and
+// H + L is the exact sum of all leaves.  So is the FP64 tree's result: every node
+// of it is a partial sum of fewer than 2^53 units, hence exact.  H + L is rounded
+// once to bf16: s = fl(H + L) plus its exact TwoSum error decides the one case s
+// alone cannot, a tie.  Both accumulators start at -0, so an all -0 input gives
+// -0 and any exact zero sum of other leaves +0, as IEEE addition in the tree gives
+// it.  Wider spreads, leaves from 2^124 up (no FP32 overflow), infinities and NaNs
+// take the FP64 tree itself, in a separate routine.
 //
 // The per-rank chains: a slot whose expert another rank owns adds w * 0 = +-0 to
 // that rank's accumulator, which changes nothing except -0 + +0 = +0 when w has a
-// clear sign bit.  Per token (the same for every column) the CTA works out, for
-// each slot, whether its owner's accumulator must first be normalised (acc + 0.0f)
-// because such a slot came after the owner's previous FMA, and for each rank
-// whether it needs that at the end.  Each slot then costs one FMA into its own
-// rank's accumulator instead of G masked FMAs.  A token with a non-finite weight
-// runs the chains literally.
+// clear sign bit.  Per token (the same for every column) one thread orders the
+// owned slots rank by rank, slot order within a rank, and marks where a rank's
+// accumulator must first be normalised (acc + 0.0f) because such a slot came after
+// its previous FMA, and where at the end.  One running accumulator then does one
+// FMA per slot, and each rank's bf16 partial comes out at the end of its run.
+// The sum above does not depend on the order of its leaves, so the run order can
+// stand in for the rank order.  A token with a non-finite weight runs the chains
+// literally.
+//
+// Conversions to and from FP64 are integer bit manipulation: bf16 -> f64 widens
+// exactly, and f64 -> bf16 rounds once to nearest even from the full 52-bit
+// fraction, never through FP32 (that would round twice).
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -97,15 +99,16 @@ __device__ __forceinline__ uint32_t f64_to_bf16_bits(double x) {
   return s | (uint32_t)q;  // q = 128 is the smallest normal, which this encodes
 }
 
-// In-place fixed tree over v[0..N): adjacent pairs per level, odd last carried.
-template <int N>
-__device__ __forceinline__ void fp64_tree(double* v) {
-  if constexpr (N > 1) {
-#pragma unroll
-    for (int i = 0; i < N / 2; ++i) v[i] = __dadd_rn(v[2 * i], v[2 * i + 1]);
-    if constexpr ((N & 1) != 0) v[N / 2] = v[N - 1];
-    fp64_tree<(N + 1) / 2>(v);
+// The fixed tree over d[0..n): adjacent pairs per level in FP64, odd last carried;
+// the bf16 of the last value.
+__device__ __forceinline__ uint32_t fp64_tree_to_bf16(double* d, int n) {
+  while (n > 1) {
+    int m = 0;
+    for (int i = 0; i + 1 < n; i += 2) d[m++] = __dadd_rn(d[i], d[i + 1]);
+    if (n & 1) d[m++] = d[n - 1];
+    n = m;
   }
+  return f64_to_bf16_bits(d[0]);
 }
 
 __host__ __device__ constexpr int ceil_log2(int n) { return n <= 1 ? 0 : 1 + ceil_log2((n + 1) / 2); }
@@ -130,281 +133,458 @@ __device__ __forceinline__ uint32_t round_pair_to_bf16(float s, float err) {
   return b;
 }
 
-// bf16(FP64 tree over the G bf16 leaves `b`).  active: leaves that may be non-zero;
-// the others are known to be +0 (a rank that owns no slot of the token).
-template <int G>
-__device__ __forceinline__ uint32_t reduce_leaves(const uint32_t* b, uint32_t active) {
-  if constexpr (G == 1) {  // no addition: the value itself (NaN as the FP64 path gives it)
-    return ((b[0] & 0x7F80u) == 0x7F80u && (b[0] & 0x7Fu)) ? 0x7FC0u : b[0];
-  }
-  constexpr int kW = 16 - ceil_log2(G);
-  constexpr uint32_t kAll = (1u << G) - 1u;
-  int e_max = 0, e_min = 255;
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    if ((active >> g) & 1u) {
-      const int e = (int)((b[g] >> 7) & 0xFFu);
-      const bool nz = (b[g] & 0x7FFFu) != 0u;
-      e_max = max(e_max, e);
-      e_min = nz ? min(e_min, max(e, 1)) : e_min;  // subnormals: the spacing of e = 1
-    }
-  }
+// One column of the exact path.  mx, mn1: the largest |leaf| bits and the
+// smallest (|leaf| bits - 1) over the present leaves (so 0xFFFF: no non-zero
+// leaf); returns false where the FP64 tree itself must decide.
+template <int kW>
+__device__ __forceinline__ bool exact_window(uint32_t mx, uint32_t mn1, uint32_t& thr) {
+  const int e_max = (int)(mx >> 7);
+  const int e_min = mn1 == 0xFFFFu ? 255 : max((int)((mn1 + 1u) >> 7), 1);  // subnormals: e = 1
   // e_max <= 250: leaves below 2^124; e = 255 (inf / NaN) fails it too
-  if (e_max <= 250 && e_max - e_min <= 2 * kW + 1) {
-    const int split = e_max - kW;  // H: e >= split (within kW of e_max), L: the rest
-    float h = ((active & kAll) == kAll) ? -0.0f : 0.0f;  // a known +0 leaf joins as +0
-    float l = -0.0f;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if ((active >> g) & 1u) {
-        const float v = __uint_as_float(b[g] << 16);
-        const bool hi = (int)((b[g] >> 7) & 0xFFu) >= split;
-        h = __fadd_rn(h, hi ? v : -0.0f);
-        l = __fadd_rn(l, hi ? -0.0f : v);
-      }
-    }
-    const float s = __fadd_rn(h, l);
-    const float bv = __fsub_rn(s, h);
-    const float err = __fadd_rn(__fsub_rn(h, __fsub_rn(s, bv)), __fsub_rn(l, bv));
-    return round_pair_to_bf16(s, err);
-  }
-  double d[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) d[g] = bf16_bits_to_f64(((active >> g) & 1u) ? b[g] : 0u);
-  fp64_tree<G>(d);
-  return f64_to_bf16_bits(d[0]);
+  if (!(e_max <= 250 && e_max - e_min <= 2 * kW + 1)) return false;
+  thr = (uint32_t)max(e_max - kW, 0) << 7;  // H: |leaf| bits >= thr (within kW of e_max)
+  return true;
 }
 
-// Per-token chain schedule (see the header).  norm_pre bit j: normalise slot j's
-// owner before its FMA; norm_end bit g: normalise rank g after the last slot;
-// literal: a weight is not finite, run the chains as written.
-struct ChainPlan {
-  uint32_t norm_pre, norm_end;
-  uint32_t active;  // ranks owning at least one slot (all ranks when shards are added)
-  int literal;
+// The exact path for both columns of the packed leaves words[i] (column 0 in the
+// low half) with bit i of `mask` set.  Any order: the sums are exact.  kW: the
+// window of one FP32 group for the largest number of leaves present.
+// no_pos_zero: no leaf outside the mask is a known +0.  Returns bit c set where
+// column c could not take the exact path (the FP64 tree must decide it).
+template <int N, int kW>
+__device__ __forceinline__ uint32_t exact_pair_sum(const uint32_t* words, uint32_t mask,
+                                                   bool no_pos_zero, uint32_t& out) {
+  uint32_t mx = 0u, mn1 = 0xFFFFFFFFu;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if ((mask >> i) & 1u) {
+      const uint32_t ab = words[i] & 0x7FFF7FFFu;  // |leaf| bits, both columns
+      mx = __vmaxu2(mx, ab);
+      mn1 = __vminu2(mn1, __vsub2(ab, 0x00010001u));  // 0 wraps to 0xFFFF
+    }
+  }
+  uint32_t thr0 = 0u, thr1 = 0u;
+  const bool ok0 = exact_window<kW>(mx & 0xFFFFu, mn1 & 0xFFFFu, thr0);
+  const bool ok1 = exact_window<kW>(mx >> 16, mn1 >> 16, thr1);
+  const uint32_t thr = thr0 | (thr1 << 16);
+  const float z = no_pos_zero ? -0.0f : 0.0f;  // a known +0 leaf joins as +0
+  float h0 = z, h1 = z, l0 = -0.0f, l1 = -0.0f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if ((mask >> i) & 1u) {
+      const uint32_t w = words[i];
+      const uint32_t m = __vcmpgeu2(w & 0x7FFF7FFFu, thr);  // 0xFFFF where the leaf is in H
+      const uint32_t m0 = (uint32_t)((int32_t)(m << 16) >> 16), m1 = (uint32_t)((int32_t)m >> 16);
+      const uint32_t v0 = w << 16, v1 = w & 0xFFFF0000u;
+      // in the group: the leaf; out of it: -0 (the identity of IEEE addition)
+      h0 = __fadd_rn(h0, __uint_as_float((v0 & m0) | (0x80000000u & ~m0)));
+      l0 = __fadd_rn(l0, __uint_as_float((v0 & ~m0) | (0x80000000u & m0)));
+      h1 = __fadd_rn(h1, __uint_as_float((v1 & m1) | (0x80000000u & ~m1)));
+      l1 = __fadd_rn(l1, __uint_as_float((v1 & ~m1) | (0x80000000u & m1)));
+    }
+  }
+  uint32_t r[2];
+  const float hs[2] = {h0, h1}, ls[2] = {l0, l1};
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const float sum = __fadd_rn(hs[c], ls[c]);
+    const float bv = __fsub_rn(sum, hs[c]);
+    const float err = __fadd_rn(__fsub_rn(hs[c], __fsub_rn(sum, bv)), __fsub_rn(ls[c], bv));
+    r[c] = round_pair_to_bf16(sum, err);
+  }
+  out = r[0] | (r[1] << 16);
+  return (ok0 ? 0u : 1u) | (ok1 ? 0u : 2u);
+}
+
+// The common case first: all present leaves non-zero and within one window of
+// S = 16 - ceil(log2 G) binades (max|leaf| < min|leaf| * 2^S), so their plain FP32
+// sum is exact in any order and rounds once to bf16.  Returns bit c set where
+// column c needs exact_pair_sum instead (a zero leaf, a wider spread, inf, NaN).
+template <int N, int kW>
+__device__ __forceinline__ uint32_t fast_pair_sum(const uint32_t* words, uint32_t mask,
+                                                  bool no_pos_zero, uint32_t& out) {
+  constexpr float kScale = (float)(1u << kW);
+  const float z = no_pos_zero ? -0.0f : 0.0f;
+  float s0 = z, s1 = z, mx0 = 0.0f, mx1 = 0.0f;
+  float mn0 = __int_as_float(0x7F800000), mn1 = mn0;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if ((mask >> i) & 1u) {
+      const float v0 = __uint_as_float(words[i] << 16);
+      const float v1 = __uint_as_float(words[i] & 0xFFFF0000u);
+      s0 = __fadd_rn(s0, v0);
+      s1 = __fadd_rn(s1, v1);
+      mx0 = fmaxf(mx0, fabsf(v0));
+      mx1 = fmaxf(mx1, fabsf(v1));
+      mn0 = fminf(mn0, fabsf(v0));
+      mn1 = fminf(mn1, fabsf(v1));
+    }
+  }
+  // mx < 2^124: no FP32 overflow, no inf; mn > 0: no zero leaf; a NaN leaf makes s NaN
+  const bool ok0 = mx0 < __int_as_float(0x7D800000) && mn0 > 0.0f && mx0 < mn0 * kScale && s0 == s0;
+  const bool ok1 = mx1 < __int_as_float(0x7D800000) && mn1 > 0.0f && mx1 < mn1 * kScale && s1 == s1;
+  const __nv_bfloat162 r = __floats2bfloat162_rn(s0, s1);
+  out = *reinterpret_cast<const uint32_t*>(&r);
+  return (ok0 ? 0u : 1u) | (ok1 ? 0u : 2u);
+}
+
+// fast_pair_sum, then exact_pair_sum for the columns it could not take.  Returns
+// bit c set where column c needs the FP64 tree itself.
+template <int N, int kW>
+__device__ __forceinline__ uint32_t leaf_pair_sum(const uint32_t* words, uint32_t mask,
+                                                  bool no_pos_zero, uint32_t& out) {
+  uint32_t fast;
+  const uint32_t miss = fast_pair_sum<N, kW>(words, mask, no_pos_zero, fast);
+  if (miss == 0u) {
+    out = fast;
+    return 0u;
+  }
+  uint32_t ex;
+  const uint32_t bad = exact_pair_sum<N, kW>(words, mask, no_pos_zero, ex);
+  const uint32_t keep = (miss & 1u ? 0u : 0xFFFFu) | (miss & 2u ? 0u : 0xFFFF0000u);
+  out = (fast & keep) | (ex & ~keep);
+  return bad & miss;
+}
+
+// Per-token schedule, the same for every column.  The owned slots visited rank
+// by rank, in slot order within a rank ("positions" p); bits over positions:
+// first of its rank's run, last of it, normalise before the FMA, normalise at the
+// end of the run.  has_run: ranks owning at least one slot.  literal: a weight is
+// not finite, run the chains as written.
+struct TokenPlan {
+  int n_pos, literal;
+  uint32_t first, last, norm_pre, norm_end, has_run;
+  int row[kMaxK];
+  int rank[kMaxK];
+  float w[kMaxK];
 };
 
 // Slots with an invalid row contribute nothing to any rank and are left out.
-__device__ __forceinline__ ChainPlan plan_chains(const int* row, const int* own, const float* w,
-                                                 int k, int G) {
-  ChainPlan p{0u, 0u, 0u, 0};
-  uint32_t started = 0u, pending = 0u;
+__device__ void build_plan(TokenPlan& P, const int* row, const int* own, const float* w, int k,
+                           int G) {
   const uint32_t all = (G >= 32) ? 0xFFFFFFFFu : ((1u << G) - 1u);
-  for (int j = 0; j < k; ++j) {
+  uint32_t started = 0u, pending = 0u, pre_slot = 0u;
+  int literal = 0;
+  for (int j = 0; j < k; ++j) {  // slot order: where a -0 must become +0
     if (row[j] < 0) continue;
-    if (!isfinite(w[j])) p.literal = 1;
-    const int o = own[j];
-    const uint32_t ob = (o >= 0) ? (1u << o) : 0u;
-    if (started & pending & ob) p.norm_pre |= 1u << j;
+    if (!isfinite(w[j])) literal = 1;
+    const uint32_t ob = own[j] >= 0 ? (1u << own[j]) : 0u;
+    if (started & pending & ob) pre_slot |= 1u << j;
     started |= ob;
     pending &= ~ob;
-    if (!signbit(w[j])) pending |= all & ~ob;  // w * 0 = +0: -0 becomes +0 in the others
+    if (!signbit(w[j])) pending |= all & ~ob;  // w * 0 = +0 reaches every other rank
   }
-  p.norm_end = started & pending;
-  p.active = started;
-  return p;
+  const uint32_t end_rank = started & pending;
+  uint32_t first = 0u, last = 0u, norm_pre = 0u, norm_end = 0u;
+  int n = 0;
+  for (int g = 0; g < G; ++g) {
+    int lastp = -1;
+    for (int j = 0; j < k; ++j) {
+      if (row[j] < 0 || own[j] != g) continue;
+      const int p = n++;
+      P.row[p] = row[j];
+      P.rank[p] = g;
+      P.w[p] = w[j];
+      if (lastp < 0) first |= 1u << p;
+      else if ((pre_slot >> j) & 1u) norm_pre |= 1u << p;
+      lastp = p;
+    }
+    if (lastp >= 0) {
+      last |= 1u << lastp;
+      if ((end_rank >> g) & 1u) norm_end |= 1u << lastp;
+    }
+  }
+  P.n_pos = n;
+  P.literal = literal;
+  P.first = first;
+  P.last = last;
+  P.norm_pre = norm_pre;
+  P.norm_end = norm_end;
+  P.has_run = started;
 }
 
-__device__ __forceinline__ float norm0(float a) { return __fadd_rn(a, 0.0f); }
+// One output element the way the section writes it: every rank's chain over all
+// slots with exact zeros, the shard, one rounding, the FP64 tree.  Used for tokens
+// with a non-finite weight and for the rare element the exact path cannot take.
+__device__ __noinline__ uint32_t literal_element(const float* __restrict__ y, const int* row,
+                                                 const int* own, const float* w, int k, int G,
+                                                 const float* __restrict__ shared, int T, int H,
+                                                 int t, int c, uint16_t* partials) {
+  double d[kMaxShards];
+  for (int g = 0; g < G; ++g) {
+    float acc = 0.0f;
+    for (int j = 0; j < k; ++j)
+      if (row[j] >= 0) acc = fmaf(w[j], own[j] == g ? y[(size_t)row[j] * H + c] : 0.0f, acc);
+    if (shared != nullptr) acc = __fadd_rn(acc, shared[((size_t)g * T + t) * H + c]);
+    const uint32_t b = f32_to_bf16_bits(acc);
+    if (partials != nullptr) partials[((size_t)g * T + t) * H + c] = (uint16_t)b;
+    d[g] = bf16_bits_to_f64(b);
+  }
+  return fp64_tree_to_bf16(d, G);
+}
 
-// One CTA per token, CPT consecutive columns per thread.
-template <int G, int CPT>
-__global__ void __launch_bounds__(128) combine_sharded_kernel(
+// One warp per token (kWarps tokens per CTA), two consecutive columns per lane
+// (a leaf's two columns share one 32-bit register).  GM >= G bounds the ranks,
+// KP >= k the slots, SHARED says whether shard outputs are added.  Column pairs
+// that the exact path cannot take are marked in shared memory and redone after
+// the main loop, so the rare FP64 routine stays out of it.  Warps synchronise
+// only among their own lanes.
+constexpr int kShardWarps = 4;
+
+struct WarpToken {
+  int row[kMaxK];
+  int own[kMaxK];
+  float w[kMaxK];
+  TokenPlan plan;
+  int any_redo;
+  uint32_t redo[16384 / 2 / 32];  // one bit per column pair (H <= 16384)
+};
+
+template <int GM, int KP, bool SHARED>
+__global__ void __launch_bounds__(kShardWarps * 32, 4) combine_sharded_kernel(
     const float* __restrict__ y, const float* __restrict__ topk_w,
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ row_of_slot,
-    const int32_t* __restrict__ owner, int T, int H, int E, int k, float scale,
+    const int32_t* __restrict__ owner, int G, int T, int H, int E, int k, float scale,
     const float* __restrict__ shared, uint16_t* __restrict__ partials, uint16_t* __restrict__ out) {
-  __shared__ int s_row[kMaxK];
-  __shared__ int s_own[kMaxK];
-  __shared__ float s_w[kMaxK];
-  __shared__ ChainPlan s_plan;
-  const int t = blockIdx.x;
+  constexpr int kW = 16 - ceil_log2(GM);  // one leaf per rank, at most GM
+  __shared__ WarpToken s_tok[kShardWarps];
+  // with shards: each lane's run-end values by rank
+  __shared__ float2 s_end[kShardWarps][SHARED ? GM : 1][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kShardWarps + warp;
+  if (t >= T) return;
+  WarpToken& W = s_tok[warp];
   const long long R = (long long)T * k;
-  if (threadIdx.x < k) {
-    const int j = threadIdx.x;
-    const int r = row_of_slot[(size_t)t * k + j];
-    const int e = topk_idx[(size_t)t * k + j];
+  if (lane < k) {
+    const int r = row_of_slot[(size_t)t * k + lane];
+    const int e = topk_idx[(size_t)t * k + lane];
     const int o = (e >= 0 && e < E) ? owner[e] : -1;
-    s_row[j] = (r >= 0 && r < R) ? r : -1;
-    s_own[j] = (o >= 0 && o < G) ? o : -1;  // -1: no rank owns the slot
-    s_w[j] = __fmul_rn(scale, topk_w[(size_t)t * k + j]);
+    W.row[lane] = (r >= 0 && r < R) ? r : -1;
+    W.own[lane] = (o >= 0 && o < G) ? o : -1;  // -1: no rank owns the slot
+    W.w[lane] = __fmul_rn(scale, topk_w[(size_t)t * k + lane]);
   }
-  __syncthreads();
-  if (threadIdx.x == 0) s_plan = plan_chains(s_row, s_own, s_w, k, G);
-  __syncthreads();
-  const ChainPlan plan = s_plan;
-  // with shards added every rank's partial may be non-zero; a literal token keeps all
-  const uint32_t active = (shared != nullptr || plan.literal) ? 0xFFFFu : plan.active;
-  int row[kMaxK], own[kMaxK];
-  float w[kMaxK];
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    row[j] = (j < k) ? s_row[j] : -1;
-    own[j] = (j < k) ? s_own[j] : -1;
-    w[j] = (j < k) ? s_w[j] : 0.0f;
-  }
-  for (int c0 = threadIdx.x * CPT; c0 < H; c0 += blockDim.x * CPT) {
-    float v[kMaxK][CPT];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (row[j] >= 0) {
-        const float* src = y + (size_t)row[j] * H + c0;
-        if constexpr (CPT == 4) {
-          const float4 q = __ldg(reinterpret_cast<const float4*>(src));
-          v[j][0] = q.x; v[j][1] = q.y; v[j][2] = q.z; v[j][3] = q.w;
-        } else {
-          const float2 q = __ldg(reinterpret_cast<const float2*>(src));
-          v[j][0] = q.x; v[j][1] = q.y;
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < CPT; ++c) v[j][c] = 0.0f;
-      }
+  for (int i = lane; i < H / 64; i += 32) W.redo[i] = 0u;
+  if (lane == 0) W.any_redo = 0;
+  __syncwarp();
+  if (lane == 0) build_plan(W.plan, W.row, W.own, W.w, k, G);
+  __syncwarp();
+  const float* sh = SHARED ? shared : nullptr;
+  if (W.plan.literal) {
+    for (int c0 = lane * 2; c0 < H; c0 += 64) {
+      const uint32_t o0 = literal_element(y, W.row, W.own, W.w, k, G, sh, T, H, t, c0, partials);
+      const uint32_t o1 = literal_element(y, W.row, W.own, W.w, k, G, sh, T, H, t, c0 + 1, partials);
+      *reinterpret_cast<uint32_t*>(out + (size_t)t * H + c0) = o0 | (o1 << 16);
     }
-    float acc[G][CPT];
+    return;
+  }
+  const int n_pos = W.plan.n_pos;
+  const uint32_t first = W.plan.first, last = W.plan.last;
+  const uint32_t norm_pre = W.plan.norm_pre, norm_end = W.plan.norm_end;
+  const uint32_t has_run = W.plan.has_run;
+  const uint32_t all = (1u << G) - 1u;
+  const uint32_t no_run = all & ~has_run;
+  int prow[KP];
+  float pw[KP];
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+  for (int p = 0; p < KP; ++p) {
+    prow[p] = (p < n_pos) ? W.plan.row[p] : 0;
+    pw[p] = (p < n_pos) ? W.plan.w[p] : 0.0f;
+  }
+  // leaves: with shards one per rank (index = rank), else the run ends (index = position)
+  constexpr int NL = SHARED ? GM : KP;
+  const uint32_t mask = SHARED ? all : last;
+  const bool no_pos_zero = SHARED || no_run == 0u;
+  // the rows of the next column pair are in flight while this one is computed
+  float2 vn[KP];
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) acc[g][c] = 0.0f;
-    if (!plan.literal) {
+  for (int p = 0; p < KP; ++p)
+    if (p < n_pos) vn[p] = __ldg(reinterpret_cast<const float2*>(y + (size_t)prow[p] * H + lane * 2));
+  for (int c0 = lane * 2; c0 < H; c0 += 64) {
+    float2 v[KP];
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < k && row[j] >= 0) {
-          const bool pre = (plan.norm_pre >> j) & 1u;
-          switch (own[j]) {  // the same value in every thread of the CTA
-#define MOE_SLOT_CASE(n)                                                     \
-  case n:                                                                    \
-    if constexpr (n < G) {                                                   \
-      _Pragma("unroll") for (int c = 0; c < CPT; ++c) {                      \
-        const float a = pre ? norm0(acc[n][c]) : acc[n][c];                  \
-        acc[n][c] = fmaf(w[j], v[j][c], a);                                  \
-      }                                                                      \
-    }                                                                        \
-    break;
-            MOE_SLOT_CASE(0) MOE_SLOT_CASE(1) MOE_SLOT_CASE(2) MOE_SLOT_CASE(3)
-            MOE_SLOT_CASE(4) MOE_SLOT_CASE(5) MOE_SLOT_CASE(6) MOE_SLOT_CASE(7)
-            MOE_SLOT_CASE(8) MOE_SLOT_CASE(9) MOE_SLOT_CASE(10) MOE_SLOT_CASE(11)
-            MOE_SLOT_CASE(12) MOE_SLOT_CASE(13) MOE_SLOT_CASE(14) MOE_SLOT_CASE(15)
-#undef MOE_SLOT_CASE
-            default:
-              break;
+    for (int p = 0; p < KP; ++p) v[p] = vn[p];
+    if (c0 + 64 < H) {
+#pragma unroll
+      for (int p = 0; p < KP; ++p)
+        if (p < n_pos)
+          vn[p] = __ldg(reinterpret_cast<const float2*>(y + (size_t)prow[p] * H + c0 + 64));
+    }
+    // shard values: issued with the rows for up to 8 ranks, later for more (registers)
+    constexpr bool kEarlyShards = SHARED && GM <= 8;
+    float2 shv[kEarlyShards ? GM : 1];
+    if constexpr (kEarlyShards) {
+#pragma unroll
+      for (int g = 0; g < GM; ++g)
+        if (g < G) shv[g] = __ldg(reinterpret_cast<const float2*>(shared + ((size_t)g * T + t) * H + c0));
+    }
+    uint32_t lf[NL];  // bf16 leaves, column c0 in the low half
+    float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+    for (int p = 0; p < KP; ++p) {
+      if (p < n_pos) {
+        // a run starts from +0; adding +0 normalises -0, adding -0 changes nothing
+        const bool fst = (first >> p) & 1u;
+        const float nz = ((norm_pre >> p) & 1u) ? 0.0f : -0.0f;
+        a0 = fmaf(pw[p], v[p].x, __fadd_rn(fst ? 0.0f : a0, nz));
+        a1 = fmaf(pw[p], v[p].y, __fadd_rn(fst ? 0.0f : a1, nz));
+        if ((last >> p) & 1u) {
+          const float ne = ((norm_end >> p) & 1u) ? 0.0f : -0.0f;
+          const float r0 = __fadd_rn(a0, ne), r1 = __fadd_rn(a1, ne);
+          if constexpr (SHARED) {
+            s_end[warp][W.plan.rank[p]][lane] = make_float2(r0, r1);
+          } else {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(r0, r1);
+            lf[p] = *reinterpret_cast<const uint32_t*>(&b);
+            if (partials != nullptr)
+              *reinterpret_cast<uint32_t*>(partials + ((size_t)W.plan.rank[p] * T + t) * H + c0) =
+                  lf[p];
           }
         }
       }
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-        if ((plan.norm_end >> g) & 1u)
-#pragma unroll
-          for (int c = 0; c < CPT; ++c) acc[g][c] = norm0(acc[g][c]);
-    } else {
-      // the chains as written: every rank, every slot, y or an exact zero
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j)
-          if (row[j] >= 0)
-#pragma unroll
-            for (int c = 0; c < CPT; ++c)
-              acc[g][c] = fmaf(w[j], own[j] == g ? v[j][c] : 0.0f, acc[g][c]);
     }
-    uint32_t pb[CPT][G];
+    if constexpr (SHARED) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (shared != nullptr) {
-        const float* sp = shared + ((size_t)g * T + t) * H + c0;
-        if constexpr (CPT == 4) {
-          const float4 q = __ldg(reinterpret_cast<const float4*>(sp));
-          acc[g][0] = __fadd_rn(acc[g][0], q.x); acc[g][1] = __fadd_rn(acc[g][1], q.y);
-          acc[g][2] = __fadd_rn(acc[g][2], q.z); acc[g][3] = __fadd_rn(acc[g][3], q.w);
-        } else {
-          const float2 q = __ldg(reinterpret_cast<const float2*>(sp));
-          acc[g][0] = __fadd_rn(acc[g][0], q.x); acc[g][1] = __fadd_rn(acc[g][1], q.y);
+      for (int g = 0; g < GM; ++g) {
+        if (g < G) {
+          // +0 for a rank without a slot, then its shard: one FP32 add, one rounding
+          const float2 e = ((has_run >> g) & 1u) ? s_end[warp][g][lane] : make_float2(0.0f, 0.0f);
+          float2 q;
+          if constexpr (kEarlyShards) q = shv[g];
+          else q = __ldg(reinterpret_cast<const float2*>(shared + ((size_t)g * T + t) * H + c0));
+          const __nv_bfloat162 b = __floats2bfloat162_rn(__fadd_rn(e.x, q.x), __fadd_rn(e.y, q.y));
+          lf[g] = *reinterpret_cast<const uint32_t*>(&b);
+          if (partials != nullptr)
+            *reinterpret_cast<uint32_t*>(partials + ((size_t)g * T + t) * H + c0) = lf[g];
         }
       }
+    } else if (partials != nullptr) {
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) pb[c][g] = f32_to_bf16_bits(acc[g][c]);
-      if (partials != nullptr) {
-        uint16_t* pp = partials + ((size_t)g * T + t) * H + c0;
-        if constexpr (CPT == 4) {
-          *reinterpret_cast<uint2*>(pp) =
-              make_uint2(pb[0][g] | (pb[1][g] << 16), pb[2][g] | (pb[3][g] << 16));
-        } else {
-          *reinterpret_cast<uint32_t*>(pp) = pb[0][g] | (pb[1][g] << 16);
-        }
-      }
+      for (int g = 0; g < GM; ++g)
+        if ((no_run >> g) & 1u)  // a rank without a slot: +0
+          *reinterpret_cast<uint32_t*>(partials + ((size_t)g * T + t) * H + c0) = 0u;
     }
-    uint32_t ob[CPT];
-#pragma unroll
-    for (int c = 0; c < CPT; ++c) ob[c] = reduce_leaves<G>(pb[c], active);
-    uint16_t* op = out + (size_t)t * H + c0;
-    if constexpr (CPT == 4) {
-      *reinterpret_cast<uint2*>(op) = make_uint2(ob[0] | (ob[1] << 16), ob[2] | (ob[3] << 16));
-    } else {
-      *reinterpret_cast<uint32_t*>(op) = ob[0] | (ob[1] << 16);
+    uint32_t o = 0u;
+    if (leaf_pair_sum<NL, kW>(lf, mask, no_pos_zero, o) != 0u) {
+      atomicOr(&W.redo[c0 >> 6], 1u << ((c0 >> 1) & 31));
+      W.any_redo = 1;
+    }
+    *reinterpret_cast<uint32_t*>(out + (size_t)t * H + c0) = o;
+  }
+  __syncwarp();
+  if (W.any_redo) {
+    for (int c0 = lane * 2; c0 < H; c0 += 64) {
+      if ((W.redo[c0 >> 6] >> ((c0 >> 1) & 31)) & 1u) {
+        const uint32_t o0 = literal_element(y, W.row, W.own, W.w, k, G, sh, T, H, t, c0, nullptr);
+        const uint32_t o1 =
+            literal_element(y, W.row, W.own, W.w, k, G, sh, T, H, t, c0 + 1, nullptr);
+        *reinterpret_cast<uint32_t*>(out + (size_t)t * H + c0) = o0 | (o1 << 16);
+      }
     }
   }
 }
 
-// out[n] = bf16(tree(partials[0..G-1][n])).  VEC: 8 elements per 16-byte vector
-// (every row base 16-byte aligned), else one element per step.
-template <int G, bool VEC>
+// The FP64 tree over element n of the G rows, from memory.
+__device__ __forceinline__ uint32_t tree_element_fp64(const uint16_t* __restrict__ partials, int G,
+                                                   long long N, long long n) {
+  double d[kMaxShards];
+  for (int g = 0; g < G; ++g) d[g] = bf16_bits_to_f64(partials[(size_t)g * N + n]);
+  return fp64_tree_to_bf16(d, G);
+}
+
+// out[n] = bf16(tree(partials[0..G-1][n])), GM >= G (FULL: G == GM).  VEC: 8
+// elements per 16-byte vector (every row base 16-byte aligned), else one element
+// per step.
+template <int GM, bool FULL, bool VEC>
 __global__ void __launch_bounds__(256) tree_reduce_kernel(const uint16_t* __restrict__ partials,
-                                                          long long N, uint16_t* __restrict__ out) {
+                                                          int G, long long N,
+                                                          uint16_t* __restrict__ out) {
+  constexpr int kW = 16 - ceil_log2(GM);
+  const uint32_t mask = FULL ? (1u << GM) - 1u : (1u << G) - 1u;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long first = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if constexpr (VEC) {
     const long long nv = N / 8;
     for (long long i = first; i < nv; i += stride) {
-      uint4 q[G];
+      uint4 q[GM];
 #pragma unroll
-      for (int g = 0; g < G; ++g)
-        q[g] = __ldg(reinterpret_cast<const uint4*>(partials + (size_t)g * N) + i);
+      for (int g = 0; g < GM; ++g)
+        if (FULL || g < G) q[g] = __ldg(reinterpret_cast<const uint4*>(partials + (size_t)g * N) + i);
       uint32_t o[4];
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        uint32_t b[G];
+      for (int w = 0; w < 4; ++w) {
+        uint32_t words[GM];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const uint32_t word = (&q[g].x)[h >> 1];
-          b[g] = (h & 1) ? (word >> 16) : (word & 0xFFFFu);
+        for (int g = 0; g < GM; ++g) words[g] = (&q[g].x)[w];
+        const uint32_t bad = leaf_pair_sum<GM, kW>(words, mask, true, o[w]);
+        if (bad != 0u) {
+          const long long n = 8 * i + 2 * w;
+          uint32_t lo = o[w] & 0xFFFFu, hi = o[w] >> 16;
+          if (bad & 1u) lo = tree_element_fp64(partials, G, N, n);
+          if (bad & 2u) hi = tree_element_fp64(partials, G, N, n + 1);
+          o[w] = lo | (hi << 16);
         }
-        const uint32_t r = reduce_leaves<G>(b, 0xFFFFu);
-        if (h & 1) o[h >> 1] |= r << 16;
-        else o[h >> 1] = r;
       }
       reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   } else {
     for (long long n = first; n < N; n += stride) {
-      uint32_t b[G];
+      uint32_t words[GM];
 #pragma unroll
-      for (int g = 0; g < G; ++g) b[g] = __ldg(partials + (size_t)g * N + n);
-      out[n] = (uint16_t)reduce_leaves<G>(b, 0xFFFFu);
+      for (int g = 0; g < GM; ++g) words[g] = (FULL || g < G) ? partials[(size_t)g * N + n] : 0u;
+      uint32_t r;
+      if (leaf_pair_sum<GM, kW>(words, mask, true, r) & 1u) r = tree_element_fp64(partials, G, N, n);
+      out[n] = (uint16_t)r;
     }
   }
 }
 
-template <int G>
-cudaError_t launch_tree_g(const uint16_t* p, long long N, uint16_t* out, bool vec, cudaStream_t s) {
+template <int GM>
+cudaError_t launch_tree_gm(const uint16_t* p, int G, long long N, uint16_t* out, bool vec,
+                           cudaStream_t s) {
   const long long units = vec ? N / 8 : N;
   if (units == 0) return cudaSuccess;
   const long long want = (units + 255) / 256;
   const int cap = device_sm_count() * 8;
   const int grid = (int)(want < cap ? want : cap);
-  if (vec) tree_reduce_kernel<G, true><<<grid, 256, 0, s>>>(p, N, out);
-  else tree_reduce_kernel<G, false><<<grid, 256, 0, s>>>(p, N, out);
+  const bool full = G == GM;
+  if (vec && full) tree_reduce_kernel<GM, true, true><<<grid, 256, 0, s>>>(p, G, N, out);
+  else if (vec) tree_reduce_kernel<GM, false, true><<<grid, 256, 0, s>>>(p, G, N, out);
+  else if (full) tree_reduce_kernel<GM, true, false><<<grid, 256, 0, s>>>(p, G, N, out);
+  else tree_reduce_kernel<GM, false, false><<<grid, 256, 0, s>>>(p, G, N, out);
   return cudaGetLastError();
 }
 
-template <int G>
-cudaError_t launch_combine_sharded_g(const float* y, const float* topk_w, const int32_t* topk_idx,
-                                     const int32_t* row_of_slot, const int32_t* owner, int T, int H,
-                                     int E, int k, float scale, const float* shared,
-                                     uint16_t* partials, uint16_t* out, cudaStream_t s) {
-  constexpr int CPT = G <= 8 ? 4 : 2;  // fewer columns per thread keep G > 8 in registers
-  combine_sharded_kernel<G, CPT><<<T, 128, 0, s>>>(y, topk_w, topk_idx, row_of_slot, owner, T, H,
-                                                   E, k, scale, shared, partials, out);
+template <int GM, int KP>
+cudaError_t launch_combine_gm(const float* y, const float* topk_w, const int32_t* topk_idx,
+                              const int32_t* row_of_slot, const int32_t* owner, int G, int T, int H,
+                              int E, int k, float scale, const float* shared, uint16_t* partials,
+                              uint16_t* out, cudaStream_t s) {
+  const int grid = (T + kShardWarps - 1) / kShardWarps;
+  if (shared != nullptr)
+    combine_sharded_kernel<GM, KP, true><<<grid, kShardWarps * 32, 0, s>>>(
+        y, topk_w, topk_idx, row_of_slot, owner, G, T, H, E, k, scale, shared, partials, out);
+  else
+    combine_sharded_kernel<GM, KP, false><<<grid, kShardWarps * 32, 0, s>>>(
+        y, topk_w, topk_idx, row_of_slot, owner, G, T, H, E, k, scale, nullptr, partials, out);
   return cudaGetLastError();
+}
+
+template <int KP>
+cudaError_t launch_combine_kp(const float* y, const float* topk_w, const int32_t* topk_idx,
+                              const int32_t* row_of_slot, const int32_t* owner, int G, int T, int H,
+                              int E, int k, float scale, const float* shared, uint16_t* partials,
+                              uint16_t* out, cudaStream_t s) {
+  if (G <= 2)
+    return launch_combine_gm<2, KP>(y, topk_w, topk_idx, row_of_slot, owner, G, T, H, E, k, scale,
+                                    shared, partials, out, s);
+  if (G <= 4)
+    return launch_combine_gm<4, KP>(y, topk_w, topk_idx, row_of_slot, owner, G, T, H, E, k, scale,
+                                    shared, partials, out, s);
+  if (G <= 8)
+    return launch_combine_gm<8, KP>(y, topk_w, topk_idx, row_of_slot, owner, G, T, H, E, k, scale,
+                                    shared, partials, out, s);
+  return launch_combine_gm<16, KP>(y, topk_w, topk_idx, row_of_slot, owner, G, T, H, E, k, scale,
+                                   shared, partials, out, s);
 }
 
 }  // namespace
@@ -413,40 +593,26 @@ cudaError_t launch_tree_reduce(const void* partials, int G, long long N, void* o
                                cudaStream_t s) {
   const uint16_t* p = static_cast<const uint16_t*>(partials);
   uint16_t* o = static_cast<uint16_t*>(out);
-  switch (G) {
-#define MOE_TREE_CASE(n) \
-  case n:                \
-    return launch_tree_g<n>(p, N, o, vec, s);
-    MOE_TREE_CASE(1) MOE_TREE_CASE(2) MOE_TREE_CASE(3) MOE_TREE_CASE(4)
-    MOE_TREE_CASE(5) MOE_TREE_CASE(6) MOE_TREE_CASE(7) MOE_TREE_CASE(8)
-    MOE_TREE_CASE(9) MOE_TREE_CASE(10) MOE_TREE_CASE(11) MOE_TREE_CASE(12)
-    MOE_TREE_CASE(13) MOE_TREE_CASE(14) MOE_TREE_CASE(15) MOE_TREE_CASE(16)
-#undef MOE_TREE_CASE
-    default:
-      return cudaErrorInvalidValue;
-  }
+  if (G < 1 || G > kMaxShards) return cudaErrorInvalidValue;
+  if (G <= 2) return launch_tree_gm<2>(p, G, N, o, vec, s);
+  if (G <= 4) return launch_tree_gm<4>(p, G, N, o, vec, s);
+  if (G <= 8) return launch_tree_gm<8>(p, G, N, o, vec, s);
+  return launch_tree_gm<16>(p, G, N, o, vec, s);
 }
 
 cudaError_t launch_combine_sharded(const float* y, const float* topk_w, const int32_t* topk_idx,
                                    const int32_t* row_of_slot, const int32_t* owner, int G, int T,
                                    int H, int E, int k, float scale, const float* shared,
                                    void* partials, void* out, cudaStream_t s) {
+  if (G < 1 || G > kMaxShards) return cudaErrorInvalidValue;
   if (T == 0) return cudaSuccess;
   uint16_t* p = static_cast<uint16_t*>(partials);
   uint16_t* o = static_cast<uint16_t*>(out);
-  switch (G) {
-#define MOE_SHARD_CASE(n)                                                                      \
-  case n:                                                                                      \
-    return launch_combine_sharded_g<n>(y, topk_w, topk_idx, row_of_slot, owner, T, H, E, k, \
-                                       scale, shared, p, o, s);
-    MOE_SHARD_CASE(1) MOE_SHARD_CASE(2) MOE_SHARD_CASE(3) MOE_SHARD_CASE(4)
-    MOE_SHARD_CASE(5) MOE_SHARD_CASE(6) MOE_SHARD_CASE(7) MOE_SHARD_CASE(8)
-    MOE_SHARD_CASE(9) MOE_SHARD_CASE(10) MOE_SHARD_CASE(11) MOE_SHARD_CASE(12)
-    MOE_SHARD_CASE(13) MOE_SHARD_CASE(14) MOE_SHARD_CASE(15) MOE_SHARD_CASE(16)
-#undef MOE_SHARD_CASE
-    default:
-      return cudaErrorInvalidValue;
-  }
+  if (k <= 8)
+    return launch_combine_kp<8>(y, topk_w, topk_idx, row_of_slot, owner, G, T, H, E, k, scale,
+                                shared, p, o, s);
+  return launch_combine_kp<kMaxK>(y, topk_w, topk_idx, row_of_slot, owner, G, T, H, E, k, scale,
+                                  shared, p, o, s);
 }
 
 }  // namespace moe
