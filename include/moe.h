@@ -257,6 +257,34 @@ moe_status moe_combine_sharded(const float* y, const float* topk_w, const int32_
                                float route_scale, const float* shared, moe_dims d, void* partials,
                                void* out, void* stream);
 
+/* Shared expert ("0 train-infer mismatch for open-weight MoE RL", section
+ * "Mixture-of-experts layers": the fixed-K projections and SwiGLU of the dense
+ * FFN; each expert rank holds one shard of it).  W_gate, W_up [H, Is] and W_down
+ * [Is, H] bf16, row-major.  Rank g's shard is intermediate columns
+ * [g*Is/G, (g+1)*Is/G) of W_gate and W_up and the same rows of W_down.
+ * Limits: Is % G == 0, (Is / G) % 128 == 0, H % 128 == 0, both <= 16384. */
+size_t moe_shared_packed_bytes(int32_t H, int32_t Is);
+
+/* One-time packing of the shared expert's G shards into the K-major layout of
+ * the grouped GEMMs (packed: moe_shared_packed_bytes, 16-byte aligned). */
+moe_status moe_prepack_shared_expert(const void* w_gate, const void* w_up, const void* w_down,
+                                     int32_t H, int32_t Is, int32_t G, void* packed,
+                                     size_t packed_bytes, void* stream);
+
+/* Workspace of moe_shared_expert (0: dimensions outside the limits). */
+size_t moe_shared_expert_workspace_bytes(int32_t T, int32_t H, int32_t Is, int32_t G);
+
+/* shared_out[g, t, :] = rank g's shard of the shared expert for token t:
+ *   gate = x[t] . W_gate[:, shard g], up = x[t] . W_up[:, shard g]   (FP32 accumulation)
+ *   h = bf16(silu(gate) * up)                                       (the only rounding)
+ *   shared_out[g, t] = h . W_down[shard g, :]                       (FP32 accumulation)
+ * x [T, H] bf16; shared_packed from moe_prepack_shared_expert; shared_out
+ * [G, T, H] fp32, ready for moe_combine_sharded.  Workspace 256-byte aligned,
+ * its first word the device status (moe_read_device_status). */
+moe_status moe_shared_expert(const void* x, const void* shared_packed, int32_t T, int32_t H,
+                             int32_t Is, int32_t G, float* shared_out, void* workspace,
+                             size_t ws_bytes, void* stream);
+
 /* The fixed expert-output reduction (same section): for every n in [0, N),
  * v = partials[0..G-1][n] (bf16, logical rank order) widened exactly to FP64;
  * each level adds adjacent pairs (v0+v1, v2+v3, ...) in FP64 and carries an odd
@@ -265,6 +293,21 @@ moe_status moe_combine_sharded(const float* y, const float* topk_w, const int32_
  * (16-byte alignment and N % 8 == 0 take the vector path); 1 <= G <= 16. */
 moe_status moe_tree_reduce_bf16(const void* partials, int32_t G, int64_t N, void* out,
                                 void* stream);
+
+/* Workspace of moe_layer_fwd_sharded (Is = 0: no shared expert; 0: dimensions
+ * outside the limits). */
+size_t moe_sharded_workspace_bytes(moe_dims d, int32_t G, int32_t Is);
+
+/* The layer as G expert ranks compute it, on one GPU: moe_layer_fwd_ex up to the
+ * expert FFN, then (shared_packed != NULL, Is > 0) moe_shared_expert, then
+ * moe_combine_sharded with owner [E] (device) and the fixed FP64 tree.
+ * 1 <= G <= 16.  Workspace: moe_sharded_workspace_bytes. */
+moe_status moe_layer_fwd_sharded(const void* x, const float* w_router, const float* bias,
+                                 const moe_router_opts* opts, const void* packed_weights,
+                                 const int32_t* owner, int32_t G, const void* shared_packed,
+                                 int32_t Is, moe_dims d, void* out, int32_t* topk_idx_out,
+                                 float* topk_w_out, int32_t* counts_out, void* workspace,
+                                 size_t ws_bytes, void* stream);
 
 /* The whole layer forward: route -> load stats -> permute -> expert FFN ->
  * combine, enqueued on one stream with no host synchronisation.

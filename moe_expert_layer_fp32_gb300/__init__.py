@@ -36,7 +36,9 @@ ABI_SYMBOLS = ("moe_workspace_bytes", "moe_packed_weight_bytes", "moe_route", "m
                "moe_set_wait_limit", "moe_route_ex", "moe_combine_ex", "moe_layer_fwd_ex",
                "moe_load_stats_ex", "moe_lpt_placement_host", "moe_rank_load_summary_host",
                "moe_permute_ex", "moe_prepack_expert_weights_ex", "moe_combine_sharded",
-               "moe_tree_reduce_bf16")
+               "moe_tree_reduce_bf16", "moe_shared_packed_bytes", "moe_prepack_shared_expert",
+               "moe_shared_expert_workspace_bytes", "moe_shared_expert",
+               "moe_sharded_workspace_bytes", "moe_layer_fwd_sharded")
 
 
 class moe_dims(ctypes.Structure):
@@ -100,6 +102,13 @@ _sig = {
     "moe_combine_sharded": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, ctypes.c_float, _vp,
                                            moe_dims, _vp, _vp, _vp]),
     "moe_tree_reduce_bf16": (ctypes.c_int, [_vp, _i32, ctypes.c_int64, _vp, _vp]),
+    "moe_shared_packed_bytes": (_sz, [_i32, _i32]),
+    "moe_prepack_shared_expert": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _sz, _vp]),
+    "moe_shared_expert_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
+    "moe_shared_expert": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "moe_sharded_workspace_bytes": (_sz, [moe_dims, _i32, _i32]),
+    "moe_layer_fwd_sharded": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
+                                             moe_dims, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -244,6 +253,41 @@ def moe_tree_reduce_bf16(partials, G, N, out, stream=None):
     """out [N] = bf16(FP64 pairwise tree over partials [G, N]) (bf16 tensors)."""
     _check("moe_tree_reduce_bf16", _lib.moe_tree_reduce_bf16(_ptr(partials), int(G), int(N),
                                                              _ptr(out), _stream(stream)))
+
+
+def moe_shared_packed_bytes(H, Is) -> int:
+    return int(_lib.moe_shared_packed_bytes(int(H), int(Is)))
+
+
+def moe_shared_expert_workspace_bytes(T, H, Is, G) -> int:
+    return int(_lib.moe_shared_expert_workspace_bytes(int(T), int(H), int(Is), int(G)))
+
+
+def moe_prepack_shared_expert(w_gate, w_up, w_down, H, Is, G, packed, stream=None):
+    nbytes = packed.numel() * packed.element_size() if isinstance(packed, torch.Tensor) else 1 << 62
+    _check("moe_prepack_shared_expert", _lib.moe_prepack_shared_expert(
+        _ptr(w_gate), _ptr(w_up), _ptr(w_down), int(H), int(Is), int(G), _ptr(packed), nbytes,
+        _stream(stream)))
+
+
+def moe_shared_expert(x, shared_packed, T, H, Is, G, shared_out, workspace, stream=None):
+    wp, wb = _ws(workspace)
+    _check("moe_shared_expert", _lib.moe_shared_expert(
+        _ptr(x), _ptr(shared_packed), int(T), int(H), int(Is), int(G), _ptr(shared_out), wp, wb,
+        _stream(stream)))
+
+
+def moe_sharded_workspace_bytes(d, G, Is=0) -> int:
+    return int(_lib.moe_sharded_workspace_bytes(d, int(G), int(Is)))
+
+
+def moe_layer_fwd_sharded(x, w_router, bias, opts, packed_weights, owner, G, shared_packed, Is, d,
+                          out, topk_idx_out, topk_w_out, counts_out, workspace, stream=None):
+    wp, wb = _ws(workspace)
+    _check("moe_layer_fwd_sharded", _lib.moe_layer_fwd_sharded(
+        _ptr(x), _ptr(w_router), _ptr(bias), _opts(opts), _ptr(packed_weights), _ptr(owner),
+        int(G), _ptr(shared_packed), int(Is), d, _ptr(out), _ptr(topk_idx_out), _ptr(topk_w_out),
+        _ptr(counts_out), wp, wb, _stream(stream)))
 
 
 def moe_load_summary_host(counts_host):

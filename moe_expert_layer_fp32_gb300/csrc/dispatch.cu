@@ -335,6 +335,18 @@ cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, 
   return cudaGetLastError();
 }
 
+namespace {
+__global__ void uniform_offsets_kernel(int32_t* offsets, int G, int T) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g <= G) offsets[g] = g * T;
+}
+}  // namespace
+
+cudaError_t launch_uniform_offsets(int32_t* offsets, int G, int T, cudaStream_t s) {
+  uniform_offsets_kernel<<<(G + 1 + 255) / 256, 256, 0, s>>>(offsets, G, T);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_copy_rows(const void* x, const int32_t* row_of_slot, int T, int H, int k,
                              void* x_perm, int32_t* status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;

@@ -90,9 +90,13 @@ struct Work {
   int b_load_row;  // first row of the B box this CTA issues
 };
 
+// a_local: every group reads A rows from 0 (one A operand shared by all groups,
+// e.g. the token rows of a shared expert split into column shards); otherwise a
+// group's A rows are its output rows.
 template <int BN, int CL>
 __device__ __forceinline__ Work decode(int u, int rank, const int* s_prefix, const int* s_off,
-                                       const int* s_mt, int E, int NT, int n_per_expert) {
+                                       const int* s_mt, int E, int NT, int n_per_expert,
+                                       int a_local) {
   // largest e with s_prefix[e] <= u (experts without work share the next prefix)
   int lo = 0, hi = E - 1;
   while (lo < hi) {
@@ -123,7 +127,7 @@ __device__ __forceinline__ Work decode(int u, int rank, const int* s_prefix, con
   }
   w.a_row0 = s_off[lo] + mt * GM;
   w.rows = min(GM, s_off[lo + 1] - w.a_row0);
-  w.a_load_row = w.a_row0 + (w.mode == 2 ? rank * (GM / 2) : 0);
+  w.a_load_row = w.a_row0 - (a_local ? s_off[lo] : 0) + (w.mode == 2 ? rank * (GM / 2) : 0);
   w.b_load_row = lo * n_per_expert + w.nt * BN + (w.mode == 1 ? rank * (BN / 2) : 0);
   return w;
 }
@@ -163,7 +167,7 @@ template <int BN, bool SWIGLU, int CL>
 __global__ void __launch_bounds__(192, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps maps, const int32_t* __restrict__ offsets,
                         int E, int R, int n_per_expert, int K, void* __restrict__ out, int out_ld,
-                        int32_t* status, long long spin_limit) {
+                        int32_t* status, long long spin_limit, int a_local) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(192, 1)
       int it = 0;  // k-blocks issued
       bool aborted = false;
       for (int u = unit0; u < total && !aborted; u += unit_step) {
-        const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, n_per_expert);
+        const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, n_per_expert, a_local);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int tcount = 0;
     for (int u = unit0; u < total; u += unit_step, ++tcount) {
-      const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, n_per_expert);
+      const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, n_per_expert, a_local);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       int ok = 1;
@@ -424,7 +428,7 @@ cudaError_t kernel_grid(int* grid) {
 template <int BN, bool SWIGLU, int CL>
 cudaError_t launch_grouped(const Maps& maps, const int32_t* offsets, int E, int R,
                            int n_per_expert, int K, void* out, int out_ld, int32_t* status,
-                           long long spin_limit, cudaStream_t s) {
+                           long long spin_limit, cudaStream_t s, int a_local = 0) {
   using C = Cfg<BN>;
   int grid = 0;
   cudaError_t err = kernel_grid<BN, SWIGLU, CL>(&grid);
@@ -444,7 +448,7 @@ cudaError_t launch_grouped(const Maps& maps, const int32_t* offsets, int E, int 
     cfg.numAttrs = 1;
   }
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<BN, SWIGLU, CL>, maps, offsets, E, R,
-                            n_per_expert, K, out, out_ld, status, spin_limit);
+                            n_per_expert, K, out, out_ld, status, spin_limit, a_local);
 }
 
 }  // namespace
@@ -453,7 +457,7 @@ int gemm_down_bn(int H) { return (H % 256 == 0) ? 256 : 128; }
 
 cudaError_t launch_gemm_gate_up(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets,
                                 int E, int R, int H, int I, void* h, int32_t* status,
-                                long long spin_limit, cudaStream_t s) {
+                                long long spin_limit, cudaStream_t s, bool a_local) {
   if (R == 0) return cudaSuccess;
   Maps m;
   if (!a.encode(&m.a128, 128) || !a.encode(&m.a64, 64) || !b.encode(&m.b_full, 256) ||
@@ -461,8 +465,10 @@ cudaError_t launch_gemm_gate_up(const GemmOperand& a, const GemmOperand& b, cons
     return cudaErrorInvalidValue;
   const int NT = (2 * I) / 256;
   if (NT % 2 == 0)
-    return launch_grouped<256, true, 2>(m, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s);
-  return launch_grouped<256, true, 1>(m, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s);
+    return launch_grouped<256, true, 2>(m, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
+                                        a_local ? 1 : 0);
+  return launch_grouped<256, true, 1>(m, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
+                                      a_local ? 1 : 0);
 }
 
 cudaError_t launch_gemm_down(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets,

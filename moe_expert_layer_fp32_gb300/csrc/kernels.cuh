@@ -42,6 +42,9 @@ cudaError_t launch_rank(const int32_t* topk_idx, int T, int k, int E, const int3
 cudaError_t launch_weighted_counts(const int32_t* topk_idx, const int32_t* q, int T, int k, int E,
                                    int64_t* out, int32_t* status, cudaStream_t s);
 
+// offsets[g] = g * T for g = 0..G (G groups of T rows each)
+cudaError_t launch_uniform_offsets(int32_t* offsets, int G, int T, cudaStream_t s);
+
 // T <= kPermBlock: counts, offsets, row_of_slot and slot_of_row in one launch
 cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, int32_t* counts,
                                   int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,
@@ -57,6 +60,12 @@ cudaError_t launch_prepack(const void* w_gate, const void* w_up, const void* w_d
                            int I, void* packed, cudaStream_t s,
                            const int32_t* slot_of_expert = nullptr);
 
+// A shared expert (W_gate, W_up [H, Is], W_down [Is, H]) packed as G experts of
+// intermediate size Is/G: expert g holds columns [g*Is/G, (g+1)*Is/G) of the gate
+// and up projections and the same rows of the down projection (layout as above).
+cudaError_t launch_prepack_shared(const void* w_gate, const void* w_up, const void* w_down, int H,
+                                  int Is, int G, void* packed, cudaStream_t s);
+
 // A bf16 row-major operand [rows, cols] of a grouped GEMM.  encode() writes a TMA
 // map of it with boxes of 64 columns x box_rows rows and 128-byte swizzle
 // (defined with the ABI, which owns the driver entry point).
@@ -67,10 +76,12 @@ struct GemmOperand {
 };
 
 // grouped GEMM-1 with the SwiGLU epilogue: a = x_perm [R, H], b = packed W1
-// [E*2I, H] -> h [R, I] bf16
+// [E*2I, H] -> h [R, I] bf16.  a_local: every group reads rows of `a` from 0
+// (one token matrix for all groups, e.g. the column shards of a shared expert).
 cudaError_t launch_gemm_gate_up(const GemmOperand& a, const GemmOperand& b,
                                 const int32_t* offsets, int E, int R, int H, int I, void* h,
-                                int32_t* status, long long spin_limit, cudaStream_t s);
+                                int32_t* status, long long spin_limit, cudaStream_t s,
+                                bool a_local = false);
 
 // grouped GEMM-2: a = h [R, I], b = packed W2 [E*H, I] -> y [R, H] fp32
 cudaError_t launch_gemm_down(const GemmOperand& a, const GemmOperand& b,

@@ -61,6 +61,21 @@ Layout layout(const moe_dims& d) {
   return L;
 }
 
+// Workspace of the sharded shared expert: status word, group offsets, h [G*T, Is/G].
+struct SharedLayout {
+  size_t status, offsets, h, total;
+};
+
+SharedLayout shared_layout(int T, int G, int Is) {
+  SharedLayout L;
+  size_t o = 0;
+  L.status = o;   o += up(kAlign);
+  L.offsets = o;  o += up(((size_t)G + 1) * 4);
+  L.h = o;        o += up((size_t)T * Is * 2);  // G * T rows of Is / G
+  L.total = o;
+  return L;
+}
+
 template <typename T>
 inline T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
@@ -75,6 +90,16 @@ moe_status check_dims(const moe_dims& d) {
   if (d.E > kMaxE || d.k > kMaxK) return MOE_ERR_UNSUPPORTED;
   if (d.H % 128 != 0 || d.I % 128 != 0 || d.H > 16384 || d.I > 16384) return MOE_ERR_UNSUPPORTED;
   if ((long long)d.T * d.k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_shared(int T, int H, int Is, int G) {
+  if (T < 0 || H <= 0 || Is <= 0 || G < 1) return MOE_ERR_INVALID_ARG;
+  if (Is % G != 0) return MOE_ERR_INVALID_ARG;
+  const int Ig = Is / G;
+  if (H % 128 != 0 || Ig % 128 != 0 || H > 16384 || Ig > 16384 || G > kMaxE)
+    return MOE_ERR_UNSUPPORTED;
+  if ((long long)G * T >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -197,6 +222,44 @@ moe_status do_expert_ffn(const void* x_perm, const int32_t* offsets, const void*
   return MOE_OK;
 }
 
+// Shared expert split into G column shards: gate/up GEMM over the same token rows
+// for every shard (a_local), then the down GEMM into shared_out [G, T, H] fp32.
+// status: the device status word the GEMMs report into.
+moe_status do_shared_expert(const void* x, const void* packed, int T, int H, int Is, int G,
+                            float* shared_out, void* ws, int32_t* status, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  const SharedLayout L = shared_layout(T, G, Is);
+  const int Ig = Is / G, R = G * T;
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  void* h = at<void>(ws, L.h);
+  const uint16_t* w1 = static_cast<const uint16_t*>(packed);
+  const uint16_t* w2 = w1 + (size_t)G * 2 * Ig * H;
+  MOE_CUDA(launch_uniform_offsets(offsets, G, T, s));
+  const GemmOperand ma{x, (uint64_t)H, (uint64_t)T};
+  const GemmOperand mb{w1, (uint64_t)H, (uint64_t)G * 2 * Ig};
+  const GemmOperand mh{h, (uint64_t)Ig, (uint64_t)R};
+  const GemmOperand md{w2, (uint64_t)Ig, (uint64_t)G * H};
+  MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, G, R, H, Ig, h, status, g_wait_limit.load(), s,
+                               true));
+  MOE_CUDA(launch_gemm_down(mh, md, offsets, G, R, H, Ig, shared_out, status, g_wait_limit.load(),
+                            s));
+  return MOE_OK;
+}
+
+// Expert ranks on one GPU: owner map, rank count, optional shared expert (packed
+// by moe_prepack_shared_expert, intermediate size Is, 0: none).
+struct ShardArgs {
+  const int32_t* owner;
+  int G;
+  const void* shared_packed;
+  int Is;
+};
+
+size_t sharded_extra_bytes(const moe_dims& d, const ShardArgs& a) {
+  if (a.Is <= 0) return 0;
+  return shared_layout(d.T, a.G, a.Is).total + up((size_t)a.G * d.T * d.H * 4);
+}
+
 moe_status check_opts(const moe_router_opts& o) {
   if (o.kind != MOE_ROUTER_SOFTMAX && o.kind != MOE_ROUTER_SIGMOID_BIAS_SELECT)
     return MOE_ERR_INVALID_ARG;
@@ -209,10 +272,20 @@ constexpr moe_router_opts kDefaultOpts = {MOE_ROUTER_SOFTMAX, 0, 1.0f};
 moe_status layer_fwd(const void* x, const float* w_router, const float* bias,
                      const moe_router_opts& opts, const void* packed_weights, const moe_dims& d,
                      void* out, int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out,
-                     void* workspace, size_t ws_bytes, cudaStream_t s, cudaEvent_t* ev) {
+                     void* workspace, size_t ws_bytes, cudaStream_t s, cudaEvent_t* ev,
+                     const ShardArgs* shard = nullptr) {
   MOE_TRY(check_dims(d));
   MOE_TRY(check_opts(opts));
   MOE_TRY(check_ws(d, workspace, ws_bytes));
+  if (shard != nullptr) {
+    if (shard->G < 1 || shard->G > kMaxShards) return MOE_ERR_UNSUPPORTED;
+    MOE_TRY(need(shard->owner));
+    if (shard->Is > 0) {
+      MOE_TRY(check_shared(d.T, d.H, shard->Is, shard->G));
+      MOE_TRY(need(shard->shared_packed));
+    }
+    if (ws_bytes < layout(d).total + sharded_extra_bytes(d, *shard)) return MOE_ERR_WORKSPACE;
+  }
   MOE_TRY(need(w_router));
   if (bias != nullptr) MOE_TRY(need(bias));
   MOE_TRY(need(packed_weights));
@@ -258,6 +331,21 @@ moe_status layer_fwd(const void* x, const float* w_router, const float* bias,
                           ev != nullptr ? ev[4] : nullptr));
   else
     MOE_TRY(mark(4));
+  if (shard != nullptr) {
+    float* shared_out = nullptr;
+    if (shard->Is > 0 && d.T > 0) {
+      void* sws = at<void>(workspace, L.total);
+      shared_out = at<float>(workspace, L.total + shared_layout(d.T, shard->G, shard->Is).total);
+      MOE_TRY(do_shared_expert(x, shard->shared_packed, d.T, d.H, shard->Is, shard->G, shared_out,
+                               sws, at<int32_t>(workspace, L.status), s));
+    }
+    MOE_TRY(mark(5));
+    if (d.T > 0)
+      MOE_CUDA(launch_combine_sharded(y, w, idx, ros, shard->owner, shard->G, d.T, d.H, d.E, d.k,
+                                      opts.route_scale, shared_out, nullptr, out, s));
+    MOE_TRY(mark(6));
+    return MOE_OK;
+  }
   MOE_TRY(mark(5));
   if (d.T > 0) MOE_CUDA(launch_combine(y, w, ros, d.T, d.H, d.k, opts.route_scale, out, s));
   MOE_TRY(mark(6));
@@ -522,6 +610,65 @@ moe_status moe_combine_ex(const float* y, const float* topk_w, const int32_t* ro
 moe_status moe_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, moe_dims d,
                        void* out, void* stream) {
   return moe_combine_ex(y, topk_w, row_of_slot, 1.0f, d, out, stream);
+}
+
+size_t moe_shared_packed_bytes(int32_t H, int32_t Is) {
+  if (H <= 0 || Is <= 0) return 0;
+  return (size_t)3 * H * Is * 2;
+}
+
+size_t moe_shared_expert_workspace_bytes(int32_t T, int32_t H, int32_t Is, int32_t G) {
+  if (check_shared(T, H, Is, G) != MOE_OK) return 0;
+  return shared_layout(T, G, Is).total;
+}
+
+moe_status moe_prepack_shared_expert(const void* w_gate, const void* w_up, const void* w_down,
+                                     int32_t H, int32_t Is, int32_t G, void* packed,
+                                     size_t packed_bytes, void* stream) {
+  MOE_TRY(check_shared(0, H, Is, G));
+  MOE_TRY(need(w_gate));
+  MOE_TRY(need(w_up));
+  MOE_TRY(need(w_down));
+  MOE_TRY(need(packed));
+  if (packed_bytes < moe_shared_packed_bytes(H, Is)) return MOE_ERR_WORKSPACE;
+  MOE_TRY(device_ok());
+  MOE_CUDA(launch_prepack_shared(w_gate, w_up, w_down, H, Is, G, packed, as_stream(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_shared_expert(const void* x, const void* shared_packed, int32_t T, int32_t H,
+                             int32_t Is, int32_t G, float* shared_out, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  MOE_TRY(check_shared(T, H, Is, G));
+  if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < shared_layout(T, G, Is).total) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need(x));
+  MOE_TRY(need(shared_packed));
+  MOE_TRY(need(shared_out));
+  MOE_TRY(device_ok());
+  return do_shared_expert(x, shared_packed, T, H, Is, G, shared_out, workspace,
+                          at<int32_t>(workspace, shared_layout(T, G, Is).status), as_stream(stream));
+}
+
+size_t moe_sharded_workspace_bytes(moe_dims d, int32_t G, int32_t Is) {
+  if (check_dims(d) != MOE_OK || G < 1 || G > kMaxShards) return 0;
+  if (Is > 0 && check_shared(d.T, d.H, Is, G) != MOE_OK) return 0;
+  const ShardArgs a{nullptr, G, nullptr, Is};
+  return layout(d).total + sharded_extra_bytes(d, a);
+}
+
+moe_status moe_layer_fwd_sharded(const void* x, const float* w_router, const float* bias,
+                                 const moe_router_opts* opts, const void* packed_weights,
+                                 const int32_t* owner, int32_t G, const void* shared_packed,
+                                 int32_t Is, moe_dims d, void* out, int32_t* topk_idx_out,
+                                 float* topk_w_out, int32_t* counts_out, void* workspace,
+                                 size_t ws_bytes, void* stream) {
+  const ShardArgs a{owner, G, shared_packed, Is};
+  return layer_fwd(x, w_router, bias, opts ? *opts : kDefaultOpts, packed_weights, d, out,
+                   topk_idx_out, topk_w_out, counts_out, workspace, ws_bytes, as_stream(stream),
+                   nullptr, &a);
 }
 
 moe_status moe_combine_sharded(const float* y, const float* topk_w, const int32_t* topk_idx,

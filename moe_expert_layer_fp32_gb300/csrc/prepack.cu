@@ -14,13 +14,15 @@
 namespace moe {
 namespace {
 
-// src: per expert a [rows x cols] row-major matrix.  Writes dst[(e, map(col)), row].
+// src: per expert a [rows x cols] matrix with row stride `ld`, expert e starting
+// `estride` elements after expert e - 1.  Writes dst[(e, map(col)), row].
 // mode 0: gate half of W1, mode 1: up half of W1, mode 2: W2.
 // slot_of_expert (optional): expert e is written to physical slot slot_of_expert[e]
 // (RoutePack's materialisation of a placement: each expert's weights move into the
 // tensors of its destination slot).
 __global__ void __launch_bounds__(256) transpose_pack_kernel(const uint16_t* __restrict__ src,
-                                                             int rows, int cols, int mode, int I,
+                                                             int rows, int cols, size_t ld,
+                                                             size_t estride, int mode, int I,
                                                              int H, uint16_t* __restrict__ dst,
                                                              const int32_t* __restrict__ slot_of_expert) {
   __shared__ uint16_t tile[32][33];
@@ -28,10 +30,10 @@ __global__ void __launch_bounds__(256) transpose_pack_kernel(const uint16_t* __r
   const int de = slot_of_expert != nullptr ? __ldg(slot_of_expert + e) : e;
   if (de < 0 || de >= (int)gridDim.z) return;  // a slot outside [0, E) is not written
   const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  const uint16_t* s = src + (size_t)e * rows * cols;
+  const uint16_t* s = src + (size_t)e * estride;
   for (int i = threadIdx.y; i < 32; i += 8) {
     const int r = r0 + i, c = c0 + threadIdx.x;
-    if (r < rows && c < cols) tile[i][threadIdx.x] = s[(size_t)r * cols + c];
+    if (r < rows && c < cols) tile[i][threadIdx.x] = s[(size_t)r * ld + c];
   }
   __syncthreads();
   for (int i = threadIdx.y; i < 32; i += 8) {
@@ -59,13 +61,31 @@ cudaError_t launch_prepack(const void* w_gate, const void* w_up, const void* w_d
   uint16_t* w2 = w1 + (size_t)E * 2 * I * H;
   dim3 block(32, 8);
   dim3 g1((I + 31) / 32, (H + 31) / 32, E);  // gate/up: [H x I] per expert
-  transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_gate), H, I, 0, I, H,
-                                             w1, slot_of_expert);
-  transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_up), H, I, 1, I, H, w1,
-                                             slot_of_expert);
+  const size_t e1 = (size_t)H * I, e2 = (size_t)I * H;
+  transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_gate), H, I, I, e1, 0,
+                                             I, H, w1, slot_of_expert);
+  transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_up), H, I, I, e1, 1, I,
+                                             H, w1, slot_of_expert);
   dim3 g2((H + 31) / 32, (I + 31) / 32, E);  // down: [I x H] per expert
-  transpose_pack_kernel<<<g2, block, 0, s>>>(static_cast<const uint16_t*>(w_down), I, H, 2, I, H,
-                                             w2, slot_of_expert);
+  transpose_pack_kernel<<<g2, block, 0, s>>>(static_cast<const uint16_t*>(w_down), I, H, H, e2, 2,
+                                             I, H, w2, slot_of_expert);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepack_shared(const void* w_gate, const void* w_up, const void* w_down, int H,
+                                  int Is, int G, void* packed, cudaStream_t s) {
+  const int Ig = Is / G;
+  uint16_t* w1 = static_cast<uint16_t*>(packed);
+  uint16_t* w2 = w1 + (size_t)G * 2 * Ig * H;
+  dim3 block(32, 8);
+  dim3 g1((Ig + 31) / 32, (H + 31) / 32, G);  // shard g: columns [g*Ig, (g+1)*Ig) of [H x Is]
+  transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_gate), H, Ig, Is, Ig,
+                                             0, Ig, H, w1, nullptr);
+  transpose_pack_kernel<<<g1, block, 0, s>>>(static_cast<const uint16_t*>(w_up), H, Ig, Is, Ig, 1,
+                                             Ig, H, w1, nullptr);
+  dim3 g2((H + 31) / 32, (Ig + 31) / 32, G);  // shard g: rows [g*Ig, (g+1)*Ig) of [Is x H]
+  transpose_pack_kernel<<<g2, block, 0, s>>>(static_cast<const uint16_t*>(w_down), Ig, H, H,
+                                             (size_t)Ig * H, 2, Ig, H, w2, nullptr);
   return cudaGetLastError();
 }
 

@@ -39,6 +39,7 @@ _lib = None
 TID_X, TID_WR, TID_WG, TID_WU, TID_WD, TID_LENGTHS = 1, 2, 3, 4, 5, 6
 # Streams used only by tests that drive one step in isolation.
 TID_Y, TID_TOPK_W, TID_TOPK_IDX, TID_X_PERM, TID_MISC = 7, 8, 9, 10, 11
+TID_SWG, TID_SWU, TID_SWD = 12, 13, 14  # shared-expert weights
 
 
 def build(force: bool = False) -> str:
@@ -160,6 +161,10 @@ WORKLOADS = {
     "packed_rl": Workload("packed_rl", T=16384, H=2048, E=128, k=8, I=768, w_std=0.02,
                           zipf_s=1.2, packed=True),
     "large": Workload("large", T=32768, H=4096, E=256, k=8, I=2048, w_std=0.01),
+    # the MoE layer of Ling-3.0-tiny (HARTS, Table 1): hidden 1,536, 128 experts,
+    # top-8, expert intermediate 512; a packed RL micro-batch of 16,384 rows
+    "ling3_tiny": Workload("ling3_tiny", T=16384, H=1536, E=128, k=8, I=512, w_std=0.02,
+                           zipf_s=1.0, packed=True),
 }
 DECODE_T = (1, 8, 64, 512, 4096)   # the fine_grained layer at these batch sizes
 
@@ -206,6 +211,15 @@ def expert_weights(wl: Workload, experts=None):
             _L().synth_normal_bf16(wl.seed, TID_WU, e * H * I, H * I, wl.w_std, _ptr(wu[i]), 0)
             _L().synth_normal_bf16(wl.seed, TID_WD, e * I * H, I * H, wl.w_std, _ptr(wd[i]), 0)
     return wg, wu, wd
+
+
+def shared_expert_weights(wl: Workload, Is: int, std: float | None = None):
+    """(W_gate [H, Is], W_up [H, Is], W_down [Is, H]) bf16 bits of a shared expert
+    of intermediate size Is for the workload's hidden size."""
+    std = wl.w_std if std is None else std
+    return (normal_bf16(wl.seed, TID_SWG, (wl.H, Is), std),
+            normal_bf16(wl.seed, TID_SWU, (wl.H, Is), std),
+            normal_bf16(wl.seed, TID_SWD, (Is, wl.H), std))
 
 
 def layer_inputs(wl: Workload, T: int | None = None) -> dict:
