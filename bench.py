@@ -43,7 +43,7 @@ METRIC = "routed tokens/s per MoE layer fwd"
 # DRAM bytes per launch of the gate/up GEMM on the large workload, from one ncu
 # capture (profiles/gemm_dram_traffic_large.md), valid while the kernel sources
 # are unchanged since the capture.
-GEMM_TRAFFIC_LARGE = {"bytes": 15184053760 + 1074163456, "sources_sha256_16": "04154435aa06698f"}
+GEMM_TRAFFIC_LARGE = {"bytes": 14936551680 + 1069988096, "sources_sha256_16": "1fac7a954b86f8f0"}
 
 
 def gemm_sources_hash():
@@ -75,7 +75,34 @@ def parse():
                         "an eager profiled pass)")
     p.add_argument("--experts", type=int, default=None,
                    help="override E of the workload (smaller cases for profiling)")
+    p.add_argument("--shards", type=int, default=0,
+                   help="run the layer as G expert ranks on one GPU (contiguous expert blocks, "
+                        "per-rank BF16 partials, fixed FP64 pairwise tree); 0: the plain layer")
+    p.add_argument("--shared-is", type=int, default=0,
+                   help="with --shards: add a shared expert of this intermediate size, split "
+                        "into G column shards (0: none)")
     return p.parse_args()
+
+
+class ShardSpec:
+    """Expert ranks of the sharded variant: G, owner map (contiguous blocks), and
+    the shared expert's intermediate size and host weights (Is = 0: none)."""
+
+    def __init__(self, wl, G, Is):
+        self.G, self.Is = G, Is
+        self.owner = (np.arange(wl.E) * G // wl.E).astype(np.int32)
+        self.shared_w = synth.shared_expert_weights(wl, Is) if Is > 0 else None
+
+    def config(self):
+        return {"ranks": self.G, "owner": "contiguous expert blocks",
+                "shared_expert_I": self.Is or None,
+                "reduction": "per-rank BF16 partials, fixed pairwise FP64 tree, one BF16 rounding"}
+
+
+def shard_spec(args, wl):
+    if args.shards <= 0:
+        return None
+    return ShardSpec(wl, args.shards, args.shared_is)
 
 
 def chosen_workload(args):
@@ -180,21 +207,22 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def workload_config(wl, world, l2_note):
+def workload_config(wl, world, l2_note, shard=None):
     return {"workload": f"{wl.name}: T={wl.T} H={wl.H} E={wl.E} k={wl.k} I={wl.I}"
                         + (f", Zipf(s={wl.zipf_s}) router bias" if wl.zipf_s else ", uniform router"),
             "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
             "routed_rows_per_step": wl.T * wl.k, "accumulate": "fp32", "router": "fp32",
             "parallelism": f"replicas x{world} (no data-path collective)", "l2": l2_note,
-            "seed": wl.seed}
+            "seed": wl.seed, "sharded": None if shard is None else shard.config()}
 
 
 # ------------------------------------------------------------ CPU oracle ---
-def oracle_sample(wl, x, wr, bias, host_w, S):
+def oracle_sample(wl, x, wr, bias, host_w, S, shard=None):
     """Runs the oracle's steps on the first S tokens; returns the seconds spent in
     oracle calls.  Expert weights are restricted to the experts those tokens use
     (every row's work is unchanged; only untouched experts are left out), and
-    gathering them is not timed."""
+    gathering them is not timed.  shard: the sharded variant (shared expert shards
+    and the sharded combine with the FP64 tree in place of the combine)."""
     import oracle
     t0 = time.perf_counter()
     idx, w = oracle.route(x[:S], wr, bias, wl.k)
@@ -208,16 +236,20 @@ def oracle_sample(wl, x, wr, bias, host_w, S):
     counts, offsets, _, _ = oracle.load_stats(sub_idx, len(experts))
     xp, ros, _ = oracle.permute(x[:S], sub_idx, offsets, len(experts))
     y = oracle.expert_ffn(xp, offsets, wg, wu, wd)
-    oracle.combine(y, w, ros)
+    if shard is None:
+        oracle.combine(y, w, ros)
+    else:
+        sh = oracle.shared_expert(x[:S], *shard.shared_w, shard.G) if shard.Is else None
+        oracle.combine_sharded(y, w, idx, ros, shard.owner, shard.G, 1.0, sh)
     return t_route + time.perf_counter() - t1
 
 
-def calibrate_sample(wl, x, wr, bias, host_w, target_s):
+def calibrate_sample(wl, x, wr, bias, host_w, target_s, shard=None):
     """Token count whose oracle run takes about target_s seconds (two probes: the
     first also warms page caches and thread start-up)."""
-    oracle_sample(wl, x, wr, bias, host_w, min(wl.T, 8))
+    oracle_sample(wl, x, wr, bias, host_w, min(wl.T, 8), shard)
     S = min(wl.T, 32)
-    t = oracle_sample(wl, x, wr, bias, host_w, S)
+    t = oracle_sample(wl, x, wr, bias, host_w, S, shard)
     return int(max(8, min(wl.T, S * target_s / max(t, 1e-3))))
 
 
@@ -236,11 +268,12 @@ def run_reference(args):
     x = synth.tokens(wl)
     wr, bias = synth.router(wl)
     host_w = host_weight_fn(wl)
+    shard = shard_spec(args, wl)
     per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
-    S = calibrate_sample(wl, x, wr, bias, host_w, per_step)
+    S = calibrate_sample(wl, x, wr, bias, host_w, per_step, shard)
     for _ in range(args.warmup):
-        oracle_sample(wl, x, wr, bias, host_w, S)
-    times = [oracle_sample(wl, x, wr, bias, host_w, S) for _ in range(args.steps)]
+        oracle_sample(wl, x, wr, bias, host_w, S, shard)
+    times = [oracle_sample(wl, x, wr, bias, host_w, S, shard) for _ in range(args.steps)]
     total = sum(times)
     value = S * wl.k * args.steps / total
     cores = os.cpu_count()
@@ -248,7 +281,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded generator)",
-            "config": workload_config(wl, 1, "host caches (CPU)"),
+            "config": workload_config(wl, 1, "host caches (CPU)", shard),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"first {S} of {wl.T} tokens per step ({S * wl.k} routed rows)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -299,14 +332,44 @@ def run_ours(args):
     x = to_dev(x_host)
     wr_d = torch.from_numpy(wr).cuda()
     bias_d = None if bias is None else torch.from_numpy(bias).cuda()
-    ws = moe.new_workspace(d)
     out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
     idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, k), dtype=torch.float32, device="cuda")
     counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    shard = shard_spec(args, wl)
+    if shard is None:
+        ws = moe.new_workspace(d)
+
+        def layer(xin, o, stream=None, evs=None):
+            if evs is None:
+                moe.moe_layer_fwd(xin, wr_d, bias_d, packed, d, o, idx, w, counts, ws, stream)
+            else:
+                moe.moe_layer_fwd_profiled(xin, wr_d, bias_d, packed, d, o, idx, w, counts, ws,
+                                           evs, stream)
+    else:
+        G, Is = shard.G, shard.Is
+        owner_d = torch.from_numpy(shard.owner).cuda()
+        shared_p = None
+        if Is:
+            shared_p = torch.empty(moe.moe_shared_packed_bytes(H, Is) // 2, dtype=torch.bfloat16,
+                                   device="cuda")
+            moe.moe_prepack_shared_expert(*[to_dev(a) for a in shard.shared_w], H, Is, G, shared_p)
+        nb = moe.moe_sharded_workspace_bytes(d, G, Is)
+        if nb == 0:
+            raise ValueError(f"sharded layer: G={G}, Is={Is} outside the limits")
+        ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+
+        def layer(xin, o, stream=None, evs=None):
+            if evs is None:
+                moe.moe_layer_fwd_sharded(xin, wr_d, bias_d, None, packed, owner_d, G, shared_p,
+                                          Is, d, o, idx, w, counts, ws, stream)
+            else:
+                moe.moe_layer_fwd_sharded_profiled(xin, wr_d, bias_d, None, packed, owner_d, G,
+                                                   shared_p, Is, d, o, idx, w, counts, ws, evs,
+                                                   stream)
 
     def step():
-        moe.moe_layer_fwd(x, wr_d, bias_d, packed, d, out, idx, w, counts, ws)
+        layer(x, out)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -328,7 +391,7 @@ def run_ours(args):
     for i in range(K):
         if flush is not None:
             flush.fill_(i & 0xFF)
-        moe.moe_layer_fwd_profiled(x, wr_d, bias_d, packed, d, out, idx, w, counts, ws, evs[i])
+        layer(x, out, None, evs[i])
     end.record()
     torch.cuda.synchronize()
     clock_info = clocks.stop()
@@ -339,6 +402,9 @@ def run_ours(args):
     total_ms = max_over_ranks(dist, own_ms, torch.device("cuda", local))
     stage_names = ["route", "load_stats", "permute", "gemm_gate_up_swiglu", "gemm_down",
                    "combine"]
+    if shard is not None:
+        stage_names[4] = "gemm_down_and_shared_expert" if shard.Is else "gemm_down"
+        stage_names[5] = "combine_sharded_fp64_tree"
     stage_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
                 for j, n in enumerate(stage_names)}
     status = moe.moe_read_device_status(ws)
@@ -372,7 +438,7 @@ def run_ours(args):
         barrier(dist, local)
         own = sum(ga[i].elapsed_time(gb[i]) for i in range(K))
         total_ms = max_over_ranks(dist, own, torch.device("cuda", local))
-        graph_note = "value timed over CUDA-graph replays of moe_layer_fwd (sum of per-replay events)"
+        graph_note = "value timed over CUDA-graph replays of the layer call (sum of per-replay events)"
         status = moe.moe_read_device_status(ws)
         if status != 0:
             raise RuntimeError(f"device status {status} after the graph replays")
@@ -399,16 +465,21 @@ def run_ours(args):
     route_flop = 2.0 * T * H * E
     perm_bytes = T * H * 2 + R * H * 2 + T * k * 4 * 3
     comb_bytes = R * H * 4 + T * H * 2 + T * k * 8
+    if shard is not None and shard.Is:
+        comb_bytes += shard.G * T * H * 4  # the shard outputs
     stages = {
         "route": {"ms": stage_ms["route"], "fp32_tflops": route_flop / stage_ms["route"] / 1e9},
         "load_stats": {"ms": stage_ms["load_stats"]},
         "permute": {"ms": stage_ms["permute"],
                     "hbm_gbs": perm_bytes / stage_ms["permute"] / 1e6},
         "gemm_gate_up_swiglu": {"ms": stage_ms["gemm_gate_up_swiglu"], "tflops": achieved},
-        "gemm_down": {"ms": stage_ms["gemm_down"],
-                      "tflops": down_flop / stage_ms["gemm_down"] / 1e9},
-        "combine": {"ms": stage_ms["combine"], "hbm_gbs": comb_bytes / stage_ms["combine"] / 1e6},
+        stage_names[4]: {"ms": stage_ms[stage_names[4]],
+                         "tflops": down_flop / stage_ms[stage_names[4]] / 1e9},
+        stage_names[5]: {"ms": stage_ms[stage_names[5]],
+                         "hbm_gbs": comb_bytes / stage_ms[stage_names[5]] / 1e6},
     }
+    if shard is not None and shard.Is:
+        stages[stage_names[4]]["note"] = "tflops counts the routed down GEMM only"
     active = int((counts > 0).sum().item())
     stream_bytes = active * 3 * H * I * 2 + T * H * 2 * 2
     weight_stream = {"active_experts": active, "bytes_per_step": stream_bytes,
@@ -416,7 +487,7 @@ def run_ours(args):
                      "peak_gbs": hbm, "frac": stream_bytes / (ms_per_step / 1e3) / 1e9 / hbm,
                      "note": "active experts' weights + tokens in/out per step, over HBM"}
     grouped = (gate_up_flop + down_flop) / ((stage_ms["gemm_gate_up_swiglu"]
-                                             + stage_ms["gemm_down"]) / 1e3) / 1e12
+                                             + stage_ms[stage_names[4]]) / 1e3) / 1e12
 
     # ---------------- e2e: host buffers, copies inside the timed region ----
     # Every step copies its tokens in from pinned host memory and its output back;
@@ -428,7 +499,8 @@ def run_ours(args):
 
     def e2e_run(n):
         moe.layer_forward_host_batches([x_pin[i & 1] for i in range(n)], wr_d, bias_d, packed, d,
-                                       [out_pin[i & 1] for i in range(n)], ws)
+                                       [out_pin[i & 1] for i in range(n)], ws,
+                                       layer=None if shard is None else layer)
 
     e2e_run(2)
     torch.cuda.synchronize()
@@ -442,17 +514,24 @@ def run_ours(args):
     barrier(dist, local)
     e2e = {"value": world * R * K / (e2e_ms / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
-           "call": "layer_forward_host_batches (moe_layer_fwd per step; pinned host tokens "
-                   "copied in and outputs copied out, transfers overlapped with compute)"}
+           "call": "layer_forward_host_batches (" + ("moe_layer_fwd" if shard is None else
+                                                      "moe_layer_fwd_sharded") +
+                   " per step; pinned host tokens copied in and outputs copied out, transfers "
+                   "overlapped with compute)"}
 
     cpu = None
     if want_cpu:
         host_w = host_weight_fn(wl, full_host)
-        S = calibrate_sample(wl, x_host, wr, bias, host_w, args.cpu_seconds)
-        t = oracle_sample(wl, x_host, wr, bias, host_w, S)
+        S = calibrate_sample(wl, x_host, wr, bias, host_w, args.cpu_seconds, shard)
+        t = oracle_sample(wl, x_host, wr, bias, host_w, S, shard)
         cpu = {"value": S * k / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"first {S} of {T} tokens ({S * k} routed rows), {t:.1f} s"}
 
+    # route 1, dispatch 4 (2 up to 256 tokens: one ranking block), gate/up 1, down 1,
+    # combine 1; the shared expert adds its offsets fill and two GEMMs
+    launches_per_step = 1 + (2 if T <= 256 else 4) + 2 + 1
+    if shard is not None and shard.Is:
+        launches_per_step += 3
     if rank == 0:
         l2 = f"inputs larger than L2 (tokens {T * H * 2 / 1e6:.0f} MB, packed weights " \
              f"{E * 3 * H * I * 2 / 1e9:.2f} GB); no flush"
@@ -462,11 +541,11 @@ def run_ours(args):
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded generator; random-init weights)",
-                "config": workload_config(wl, world, l2),
+                "config": workload_config(wl, world, l2, shard),
                 "tokens_per_s": world * T * K / (total_ms / 1e3),
                 "roofline": roofline, "grouped_gemm_tflops": grouped, "stages": stages,
                 "weight_stream": weight_stream, "graph": graph_note,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 8 * K,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * K,
                 "clocks": clock_info}
         print(json.dumps(line))
     if dist is not None:

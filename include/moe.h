@@ -309,6 +309,16 @@ moe_status moe_layer_fwd_sharded(const void* x, const float* w_router, const flo
                                  float* topk_w_out, int32_t* counts_out, void* workspace,
                                  size_t ws_bytes, void* stream);
 
+/* moe_layer_fwd_sharded recording 7 events on `stream` (as moe_layer_fwd_profiled:
+ * before route, after route, after load stats, after permute, after the gate/up
+ * GEMM, after the down GEMM and the shared expert, after the sharded combine). */
+moe_status moe_layer_fwd_sharded_profiled(
+    const void* x, const float* w_router, const float* bias, const moe_router_opts* opts,
+    const void* packed_weights, const int32_t* owner, int32_t G, const void* shared_packed,
+    int32_t Is, moe_dims d, void* out, int32_t* topk_idx_out, float* topk_w_out,
+    int32_t* counts_out, void* workspace, size_t ws_bytes, void* stream, void* const* events,
+    int32_t n_events);
+
 /* The whole layer forward: route -> load stats -> permute -> expert FFN ->
  * combine, enqueued on one stream with no host synchronisation.
  *   x [T, H] bf16; w_router [H, E] fp32; bias [E] fp32 or NULL; packed_weights

@@ -38,7 +38,8 @@ ABI_SYMBOLS = ("moe_workspace_bytes", "moe_packed_weight_bytes", "moe_route", "m
                "moe_permute_ex", "moe_prepack_expert_weights_ex", "moe_combine_sharded",
                "moe_tree_reduce_bf16", "moe_shared_packed_bytes", "moe_prepack_shared_expert",
                "moe_shared_expert_workspace_bytes", "moe_shared_expert",
-               "moe_sharded_workspace_bytes", "moe_layer_fwd_sharded")
+               "moe_sharded_workspace_bytes", "moe_layer_fwd_sharded",
+               "moe_layer_fwd_sharded_profiled")
 
 
 class moe_dims(ctypes.Structure):
@@ -109,6 +110,9 @@ _sig = {
     "moe_sharded_workspace_bytes": (_sz, [moe_dims, _i32, _i32]),
     "moe_layer_fwd_sharded": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
                                              moe_dims, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_layer_fwd_sharded_profiled": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
+                                                      _i32, moe_dims, _vp, _vp, _vp, _vp, _vp,
+                                                      _sz, _vp, _vp, _i32]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -290,6 +294,26 @@ def moe_layer_fwd_sharded(x, w_router, bias, opts, packed_weights, owner, G, sha
         _ptr(counts_out), wp, wb, _stream(stream)))
 
 
+def _event_array(events, stream):
+    for e in events:
+        if e.cuda_event == 0:  # torch creates the CUDA event on its first record
+            e.record(torch.cuda.current_stream() if stream is None else stream)
+    return (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+
+
+def moe_layer_fwd_sharded_profiled(x, w_router, bias, opts, packed_weights, owner, G,
+                                   shared_packed, Is, d, out, topk_idx_out, topk_w_out, counts_out,
+                                   workspace, events, stream=None):
+    """moe_layer_fwd_sharded with 7 torch.cuda.Event(enable_timing=True) recorded at
+    the step boundaries (as moe_layer_fwd_profiled)."""
+    wp, wb = _ws(workspace)
+    arr = _event_array(events, stream)
+    _check("moe_layer_fwd_sharded_profiled", _lib.moe_layer_fwd_sharded_profiled(
+        _ptr(x), _ptr(w_router), _ptr(bias), _opts(opts), _ptr(packed_weights), _ptr(owner),
+        int(G), _ptr(shared_packed), int(Is), d, _ptr(out), _ptr(topk_idx_out), _ptr(topk_w_out),
+        _ptr(counts_out), wp, wb, _stream(stream), arr, len(events)))
+
+
 def moe_load_summary_host(counts_host):
     """(imbalance max/mean - 1, cv) from host counts (sequence or numpy array)."""
     import numpy as np
@@ -338,10 +362,7 @@ def moe_layer_fwd_profiled(x, w_router, bias, packed_weights, d, out, topk_idx_o
     boundaries (before route, after route, load stats, permute, gate/up GEMM,
     down GEMM, combine)."""
     wp, wb = _ws(workspace)
-    for e in events:
-        if e.cuda_event == 0:  # torch creates the CUDA event on its first record
-            e.record(torch.cuda.current_stream() if stream is None else stream)
-    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    arr = _event_array(events, stream)
     _check("moe_layer_fwd_profiled", _lib.moe_layer_fwd_profiled(
         _ptr(x), _ptr(w_router), _ptr(bias), _ptr(packed_weights), d, _ptr(out),
         _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), wp, wb, _stream(stream), arr,
@@ -394,7 +415,7 @@ def layer_forward(x, w_router, bias, packed, d, workspace, stream=None, want_rou
 
 
 def layer_forward_host_batches(x_host_batches, w_router, bias, packed, d, out_host_batches,
-                               workspace, stream=None):
+                               workspace, stream=None, layer=None):
     """Forward a sequence of token batches that live in pinned host memory, writing each
     batch's output back to pinned host memory.
 
@@ -402,6 +423,8 @@ def layer_forward_host_batches(x_host_batches, w_router, bias, packed, d, out_ho
     while batch i runs (moe_layer_fwd on `stream`, default the current stream), and
     batch i's output is copied back on a second copy stream while batch i+1 runs.
     Two device buffers per direction rotate.  Every batch must have d.T tokens.
+    layer: optional callable (x_dev, out_dev, stream) that runs one forward in place
+    of moe_layer_fwd (e.g. moe_layer_fwd_sharded with its own arguments bound).
     Returns once all work is enqueued; synchronise `stream` (or the last event) to
     read the outputs.
     """
@@ -425,8 +448,11 @@ def layer_forward_host_batches(x_host_batches, w_router, bias, packed, d, out_ho
         compute.wait_event(copied_in[b])
         if used[b]:
             compute.wait_event(copied_out[b])  # batch i-2's output has left o_dev[b]
-        moe_layer_fwd(x_dev[b], w_router, bias, packed, d, o_dev[b], None, None, None, workspace,
-                      compute)
+        if layer is None:
+            moe_layer_fwd(x_dev[b], w_router, bias, packed, d, o_dev[b], None, None, None,
+                          workspace, compute)
+        else:
+            layer(x_dev[b], o_dev[b], compute)
         computed[b].record(compute)
         d2h.wait_event(computed[b])
         with torch.cuda.stream(d2h):

@@ -742,6 +742,24 @@ moe_status moe_layer_fwd_profiled(const void* x, const float* w_router, const fl
                    counts_out, workspace, ws_bytes, as_stream(stream), ev);
 }
 
+moe_status moe_layer_fwd_sharded_profiled(
+    const void* x, const float* w_router, const float* bias, const moe_router_opts* opts,
+    const void* packed_weights, const int32_t* owner, int32_t G, const void* shared_packed,
+    int32_t Is, moe_dims d, void* out, int32_t* topk_idx_out, float* topk_w_out,
+    int32_t* counts_out, void* workspace, size_t ws_bytes, void* stream, void* const* events,
+    int32_t n_events) {
+  if (n_events != 7 || events == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaEvent_t ev[7];
+  for (int i = 0; i < 7; ++i) {
+    if (events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+    ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  const ShardArgs a{owner, G, shared_packed, Is};
+  return layer_fwd(x, w_router, bias, opts ? *opts : kDefaultOpts, packed_weights, d, out,
+                   topk_idx_out, topk_w_out, counts_out, workspace, ws_bytes, as_stream(stream),
+                   ev, &a);
+}
+
 moe_status moe_set_wait_limit(long long cycles) {
   g_wait_limit.store(cycles > 0 ? cycles : kSpinLimitCycles);
   return MOE_OK;

@@ -162,9 +162,11 @@ WORKLOADS = {
                           zipf_s=1.2, packed=True),
     "large": Workload("large", T=32768, H=4096, E=256, k=8, I=2048, w_std=0.01),
     # the MoE layer of Ling-3.0-tiny (HARTS, Table 1): hidden 1,536, 128 experts,
-    # top-8, expert intermediate 512; a packed RL micro-batch of 16,384 rows
+    # top-8, expert intermediate 512; a packed RL micro-batch of 16,384 rows; no
+    # popularity bias (HARTS keeps expert loads balanced through its loss and bias
+    # updates)
     "ling3_tiny": Workload("ling3_tiny", T=16384, H=1536, E=128, k=8, I=512, w_std=0.02,
-                           zipf_s=1.0, packed=True),
+                           packed=True),
 }
 DECODE_T = (1, 8, 64, 512, 4096)   # the fine_grained layer at these batch sizes
 
