@@ -149,3 +149,24 @@ def test_layer_equals_step_by_step_calls(moe, name):
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(ws) == 0
     np.testing.assert_array_equal(bits(out), out_layer)
+
+
+def test_batch_invariance_across_gemm_variants(cuda_ok):
+    """The down GEMM runs as a pair of CTAs (one M=256 MMA) from 512 rows per expert
+    on average, and as single CTAs below; the fine_grained layer crosses that line
+    between T = 4095 and T = 4096.  Each token's output must not change."""
+    import moe_expert_layer_fp32_gb300 as moe
+    from gpu_util import weights
+    wl = synth.WORKLOADS["fine_grained"]
+    W = weights(wl)
+    wr, bias = synth.router(wl)
+    x = synth.tokens(wl, 4096)
+    outs = []
+    for T in (4095, 4096):
+        d = moe.dims(T, wl.H, wl.E, wl.k, wl.I)
+        ws = moe.new_workspace(d)
+        out = moe.layer_forward(dev_bf16(x[:T]), dev(wr), dev(bias), W.packed, d, ws)
+        torch.cuda.synchronize()
+        assert moe.moe_read_device_status(ws) == 0
+        outs.append(bits(out))
+    np.testing.assert_array_equal(outs[0], outs[1][:4095])
