@@ -119,8 +119,11 @@ __device__ __forceinline__ Work decode(int u, int rank, const int* s_prefix, con
   } else {
     const int nB = (s_mt[lo] >> 1) * NT;
     if (local < nB) {
-      const int mp = local / NT;
-      w.nt = local - mp * NT;
+      // column-tile-major: consecutive clusters share one B tile (2 MB of weights)
+      // while it is in L2; the expert's rows (A) stay in L2 across its column tiles
+      const int MP = s_mt[lo] >> 1;
+      w.nt = local / MP;
+      const int mp = local - w.nt * MP;
       mt = 2 * mp + rank;
       w.mode = 1;
     } else {
