@@ -339,6 +339,154 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
   }
 }
 
+// --------------------------------------------------- large T, 2D warp tiles ---
+// route_tile_kernel: one CTA = BT = 8192/EP tokens x EP experts, 128 threads, each
+// thread an 8-token x 8-expert block of logits.  A warp covers LT*8 tokens x
+// LE*8 experts (LE = 8 lanes along experts when EP >= 64); a lane's tokens and
+// experts are two runs of four, so each of its four 16-byte shared-memory loads
+// per hidden column reads one contiguous run with the other lanes (no bank
+// conflicts) and every W_r value is read by a quarter of the lanes the 1D layout
+// needs.  Used for 256 experts once T gives every SM a CTA; the logits are the
+// same FMA chains as in route_kernel, so the bits do not depend on the kernel
+// chosen.
+template <int EP>
+struct TileCfg {
+  static constexpr int BT = 8192 / EP;
+  static constexpr int HK = (EP >= 256) ? 16 : 32;
+  static constexpr int XL = BT + 4;
+  static constexpr int LE = (EP / 8 < 8) ? EP / 8 : 8;  // lanes along experts
+  static constexpr int LT = 32 / LE;                    // lanes along tokens
+  static constexpr int WE = (EP / 8) / LE;              // warps along experts
+  static constexpr int WT = (NTHR / 32) / WE;           // warps along tokens
+  static_assert(WT * LT * 8 == BT, "tile");
+  static constexpr int w_floats = NST * HK * EP;
+  static constexpr int xst_halves = NST * BT * HK;
+  static constexpr int xs_floats = HK * XL;
+  static constexpr int ring_bytes = 4 * w_floats + 2 * xst_halves + 4 * xs_floats;
+  static constexpr int logit_bytes = 4 * BT * (EP + 1);
+  static constexpr int bytes = ring_bytes > logit_bytes ? ring_bytes : logit_bytes;
+};
+
+template <int EP, int KIND>
+__global__ void __launch_bounds__(NTHR, 4) route_tile_kernel(const uint16_t* __restrict__ x,
+                                                             const float* __restrict__ wr,
+                                                             const float* __restrict__ bias, int T,
+                                                             int H, int E, int k, int wbf16,
+                                                             int32_t* __restrict__ topk_idx,
+                                                             float* __restrict__ topk_w) {
+  using C = TileCfg<EP>;
+  constexpr int BTT = C::BT, HK = C::HK, XL = C::XL, LE = C::LE, LT = C::LT, WE = C::WE;
+  extern __shared__ float4 smem_f4[];
+  float* ws = reinterpret_cast<float*>(smem_f4);                      // [NST][HK][EP]
+  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + NST * HK * EP);    // [NST][BTT][HK]
+  float* xs = reinterpret_cast<float*>(xst + NST * BTT * HK);         // [HK][XL]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.x * BTT;
+  const int nchunks = H / HK;
+  // this thread's tokens: tb + tok(i); experts: eb + exp(j)
+  const int tb = (warp / WE) * (LT * 8) + (lane / LE) * 4;
+  const int eb = (warp % WE) * (LE * 8) + (lane % LE) * 4;
+  auto tok = [](int i) { return i < 4 ? i : 4 * LT + i - 4; };
+  auto ex = [](int j) { return j < 4 ? j : 4 * LE + j - 4; };
+
+  if (E < EP) {
+    for (int i = tid; i < NST * HK * EP; i += NTHR)
+      if ((i % EP) >= E) ws[i] = 0.0f;
+  }
+  auto issue_chunk = [&](int c) {
+    if (c < nchunks) {
+      const int buf = c % NST;
+      const int h0 = c * HK;
+      float* wdst = ws + buf * HK * EP;
+      const float* wsrc = wr + (size_t)h0 * E;
+      if (E == EP) {
+#pragma unroll
+        for (int i = tid; i < HK * EP / 4; i += NTHR) cp_async_16(wdst + 4 * i, wsrc + 4 * i, 16);
+      } else if ((E % 4) == 0) {
+        for (int i = tid; i < HK * E / 4; i += NTHR) {
+          const int f = 4 * i;
+          cp_async_16(wdst + (f / E) * EP + (f % E), wsrc + f, 16);
+        }
+      } else {
+        for (int i = tid; i < HK * E; i += NTHR)
+          cp_async_4(wdst + (i / E) * EP + (i % E), wsrc + i);
+      }
+      uint16_t* xdst = xst + buf * BTT * HK;
+      constexpr int PPR = HK / 8;
+      for (int i = tid; i < BTT * PPR; i += NTHR) {
+        const int r = i / PPR, pc = i % PPR;
+        const int t = t0 + r;
+        const uint16_t* src = (t < T) ? x + (size_t)t * H + h0 + 8 * pc : x;
+        cp_async_16(xdst + r * HK + 8 * pc, src, (t < T) ? 16 : 0);
+      }
+    }
+    cp_async_commit();
+  };
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+#pragma unroll
+  for (int c = 0; c < NST - 1; ++c) issue_chunk(c);
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = c % NST;
+    issue_chunk(c + NST - 1);
+    cp_async_wait<NST - 1>();
+    __syncthreads();
+    for (int i = tid; i < BTT * HK / 4; i += NTHR) {
+      const int r = i / (HK / 4), hq = (i % (HK / 4)) * 4;
+      const uint2 v = *reinterpret_cast<const uint2*>(xst + buf * BTT * HK + r * HK + hq);
+      xs[(hq + 0) * XL + r] = bf16_lo(v.x);
+      xs[(hq + 1) * XL + r] = bf16_hi(v.x);
+      xs[(hq + 2) * XL + r] = bf16_lo(v.y);
+      xs[(hq + 3) * XL + r] = bf16_hi(v.y);
+    }
+    __syncthreads();
+    const float* wsb = ws + buf * HK * EP;
+#pragma unroll 4
+    for (int hh = 0; hh < HK; ++hh) {
+      const float4 xa = *reinterpret_cast<const float4*>(xs + hh * XL + tb);
+      const float4 xb = *reinterpret_cast<const float4*>(xs + hh * XL + tb + 4 * LT);
+      const float4 wa = *reinterpret_cast<const float4*>(wsb + hh * EP + eb);
+      const float4 wb = *reinterpret_cast<const float4*>(wsb + hh * EP + eb + 4 * LE);
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+
+  constexpr int LLD = EP + 1;
+  const bool add_bias = KIND == 0 && bias != nullptr;
+  float* ls = reinterpret_cast<float*>(smem_f4);  // [BTT][LLD], over the drained ring
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = eb + ex(j);
+    const float b = (add_bias && e < E) ? __ldg(bias + e) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float l = acc[i][j];
+      if (add_bias) l = __fadd_rn(l, b);
+      ls[(tb + tok(i)) * LLD + e] = l;
+    }
+  }
+  __syncthreads();
+  for (int tl = warp; tl < BTT; tl += NTHR / 32) {
+    const int t = t0 + tl;
+    if (t >= T) break;
+    route_one_token<EP, KIND>(ls + tl * LLD, KIND == 1 ? bias : nullptr, E, k, wbf16, lane, t,
+                              topk_idx, topk_w);
+  }
+}
+
 // ------------------------------------------------------------- small T ---
 constexpr int SNST = 6;    // ring depth: ~100 KB of W_r in flight per CTA
 
@@ -486,6 +634,27 @@ cudaError_t launch_ep(const void* x, const float* wr, const float* bias, int T, 
     if (T == 2) return launch_small<EP, 2, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
     if (T <= 4) return launch_small<EP, 4, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
     return launch_small<EP, 8, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+  }
+  if constexpr (EP == 256) {
+    // 2D tiles once T gives every SM at least one CTA.  Measured on GB300: 5% faster
+    // than route_kernel for 256 experts; for 64 and 128 experts (fewer experts per
+    // token, larger token tiles) it was 15-45% slower, so those keep route_kernel.
+    using TC = TileCfg<EP>;
+    int sms = device_sm_count();
+    if ((long long)T >= (long long)sms * TC::BT) {
+      static bool tattr[64] = {};
+      int dv = 0;
+      cudaGetDevice(&dv);
+      if (dv < 64 && !tattr[dv]) {
+        cudaError_t e = cudaFuncSetAttribute(route_tile_kernel<EP, KIND>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, TC::bytes);
+        if (e != cudaSuccess) return e;
+        tattr[dv] = true;
+      }
+      route_tile_kernel<EP, KIND><<<(T + TC::BT - 1) / TC::BT, NTHR, TC::bytes, s>>>(
+          static_cast<const uint16_t*>(x), wr, bias, T, H, E, k, wbf16, idx, w);
+      return cudaGetLastError();
+    }
   }
   constexpr int smem = RouteCfg<EP>::bytes;
   static bool attr_set[64] = {};

@@ -40,7 +40,8 @@ def gpu_route(moe, x, wr, bias, d, opts):
 
 
 @pytest.mark.parametrize("name,T", [("fine_grained", 4096), ("fine_grained", 64),
-                                    ("fine_grained", 3), ("large", 2048), ("tiny", 256)])
+                                    ("fine_grained", 3), ("large", 2048), ("large", 5000),
+                                    ("tiny", 256)])
 @pytest.mark.parametrize("wbf16", [False, True])
 def test_sigmoid_router_bit_exact(moe, name, T, wbf16):
     wl = synth.WORKLOADS[name]

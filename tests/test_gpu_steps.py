@@ -123,3 +123,25 @@ def test_combine(moe, case):
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
     moe.moe_combine(dev(y), dev(case["w"]), dev(ros_o), d, out)
     np.testing.assert_array_equal(bits(out), oracle.combine(y, case["w"], ros_o))
+
+
+def test_route_kernels_agree_bitwise(moe):
+    """With 256 experts the router switches to 2D-tiled CTAs once every SM gets
+    one (T >= 32 x SMs, 4864 on 152 SMs); every logit is the same FMA chain in
+    both kernels, so a token's experts and weights must be the same bits either
+    side of the switch."""
+    wl = synth.WORKLOADS["large"]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Ts = (32 * sms - 1, 32 * sms + 96)
+    x = synth.tokens(wl, Ts[1])
+    wr, bias = synth.router(wl)
+    got = []
+    for T in Ts:
+        d = moe.dims(T, wl.H, wl.E, wl.k, wl.I)
+        idx = torch.empty((T, wl.k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, wl.k), dtype=torch.float32, device="cuda")
+        moe.moe_route(dev_bf16(x[:T]), dev(wr), None if bias is None else dev(bias), d, idx, w)
+        got.append((idx.cpu().numpy(), w.cpu().numpy()))
+    n = Ts[0]
+    np.testing.assert_array_equal(got[0][0], got[1][0][:n])
+    np.testing.assert_array_equal(got[0][1].view(np.uint32), got[1][1][:n].view(np.uint32))
