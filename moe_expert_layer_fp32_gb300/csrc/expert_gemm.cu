@@ -99,8 +99,7 @@ struct Work {
 // group's A rows are its output rows.
 template <int BN, int CL>
 __device__ __forceinline__ Work decode(int u, int rank, const int* s_prefix, const int* s_off,
-                                       const int* s_mt, int E, int NT, int n_per_expert,
-                                       int a_local) {
+                                       const int* s_mt, int E, int NT, int KB, int a_local) {
   // largest e with s_prefix[e] <= u (experts without work share the next prefix)
   int lo = 0, hi = E - 1;
   while (lo < hi) {
@@ -135,7 +134,9 @@ __device__ __forceinline__ Work decode(int u, int rank, const int* s_prefix, con
   w.a_row0 = s_off[lo] + mt * GM;
   w.rows = min(GM, s_off[lo + 1] - w.a_row0);
   w.a_load_row = w.a_row0 - (a_local ? s_off[lo] : 0) + (w.mode == 2 ? rank * (GM / 2) : 0);
-  w.b_load_row = lo * n_per_expert + w.nt * BN + (w.mode == 1 ? rank * (BN / 2) : 0);
+  // B is packed box by box: (expert, column tile, k-block) -> BN contiguous rows of
+  // 64 K values; this is the box row of k-block 0 (k-block kb adds kb * BN)
+  w.b_load_row = (lo * NT + w.nt) * KB * BN + (w.mode == 1 ? rank * (BN / 2) : 0);
   return w;
 }
 
@@ -146,7 +147,14 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long 
   return true;
 }
 
-__device__ __forceinline__ float silu_f32(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+// silu(g) = g / (1 + exp(-g)) on the special-function unit (ex2.approx, rcp.approx):
+// a few FP32 ulps from the correctly rounded value, which the one BF16 rounding of
+// h that follows mostly absorbs; the same instructions run for every T.  The IEEE
+// division and the library exp made the SwiGLU epilogue about 21 us per 128 x 256
+// tile, longer than the main loop for K = 2048.
+__device__ __forceinline__ float silu_f32(float g) {
+  return __fdividef(g, __fadd_rn(1.0f, __expf(-g)));
+}
 
 // One warp writes a 32-row x 128-byte block whose row i (i = lane) it holds in
 // registers: the rows go through shared memory so that every global store
@@ -298,7 +306,7 @@ __global__ void __launch_bounds__(192, 1)
       int it = 0;  // k-blocks issued
       bool aborted = false;
       for (int u = unit0; u < total && !aborted; u += unit_step) {
-        const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, n_per_expert, a_local);
+        const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, KB, a_local);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -316,10 +324,10 @@ __global__ void __launch_bounds__(192, 1)
             tma_load_2d(&maps.a128, a_dst, &full[s], kb * GK, w.a_load_row);
           }
           if (w.mode == 1) {
-            tma_load_2d_multicast(&maps.b_half, b_dst + rank * (BN / 2) * 128, &full[s], kb * GK,
-                                  w.b_load_row, 0x3);
+            tma_load_2d_multicast(&maps.b_half, b_dst + rank * (BN / 2) * 128, &full[s], 0,
+                                  w.b_load_row + kb * BN, 0x3);
           } else {
-            tma_load_2d(&maps.b_full, b_dst, &full[s], kb * GK, w.b_load_row);
+            tma_load_2d(&maps.b_full, b_dst, &full[s], 0, w.b_load_row + kb * BN);
           }
         }
       }
@@ -372,7 +380,7 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int tcount = 0;
     for (int u = unit0; u < total; u += unit_step, ++tcount) {
-      const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, n_per_expert, a_local);
+      const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, KB, a_local);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       int ok = 1;
@@ -438,7 +446,7 @@ struct PairWork {
 
 template <int BN>
 __device__ __forceinline__ PairWork decode_pair(int u, int rank, const int* s_prefix,
-                                                const int* s_off, int E, int NT, int n_per_expert,
+                                                const int* s_off, int E, int NT, int KB,
                                                 int a_local) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
@@ -453,7 +461,7 @@ __device__ __forceinline__ PairWork decode_pair(int u, int rank, const int* s_pr
   w.a_row0 = s_off[lo] + mt * (2 * GM) + rank * GM;
   w.rows = min(GM, max(0, s_off[lo + 1] - w.a_row0));
   w.a_load_row = w.a_row0 - (a_local ? s_off[lo] : 0);
-  w.b_load_row = lo * n_per_expert + w.nt * BN + rank * (BN / 2);
+  w.b_load_row = (lo * NT + w.nt) * KB * BN + rank * (BN / 2);  // k-block kb adds kb * BN
   return w;
 }
 
@@ -534,7 +542,7 @@ __global__ void __launch_bounds__(192, 1)
       int it = 0;
       bool aborted = false;
       for (int u = unit0; u < total && !aborted; u += unit_step) {
-        const PairWork w = decode_pair<BN>(u, rank, s_prefix, s_off, E, NT, n_per_expert, a_local);
+        const PairWork w = decode_pair<BN>(u, rank, s_prefix, s_off, E, NT, KB, a_local);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -545,7 +553,7 @@ __global__ void __launch_bounds__(192, 1)
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
           const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
           tma_load_2d_pair(&maps.a128, sA + s * C::A_BYTES, bar, kb * GK, w.a_load_row);
-          tma_load_2d_pair(&maps.b_half, sB + s * C::B_BYTES, bar, kb * GK, w.b_load_row);
+          tma_load_2d_pair(&maps.b_half, sB + s * C::B_BYTES, bar, 0, w.b_load_row + kb * BN);
         }
       }
       if (aborted && rank == 0) {
@@ -596,7 +604,7 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int tcount = 0;
     for (int u = unit0; u < total; u += unit_step, ++tcount) {
-      const PairWork w = decode_pair<BN>(u, rank, s_prefix, s_off, E, NT, n_per_expert, a_local);
+      const PairWork w = decode_pair<BN>(u, rank, s_prefix, s_off, E, NT, KB, a_local);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       int ok = 1;

@@ -212,9 +212,10 @@ moe_status do_expert_ffn(const void* x_perm, const int32_t* offsets, const void*
   const uint16_t* w1 = static_cast<const uint16_t*>(packed);
   const uint16_t* w2 = w1 + (size_t)d.E * 2 * d.I * d.H;
   const GemmOperand ma{x_perm, (uint64_t)d.H, (uint64_t)R};
-  const GemmOperand mb{w1, (uint64_t)d.H, (uint64_t)d.E * 2 * d.I};
+  // packed weights are box-tiled: 64 K values per row, (expert, column tile, k-block) boxes
+  const GemmOperand mb{w1, 64, (uint64_t)d.E * 2 * d.I * (d.H / 64)};
   const GemmOperand mh{h, (uint64_t)d.I, (uint64_t)R};
-  const GemmOperand md{w2, (uint64_t)d.I, (uint64_t)d.E * d.H};
+  const GemmOperand md{w2, 64, (uint64_t)d.E * d.H * (d.I / 64)};
   MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, d.E, R, d.H, d.I, h, status, g_wait_limit.load(), s));
   if (after_gate_up != nullptr) MOE_CUDA(cudaEventRecord(after_gate_up, s));
   MOE_CUDA(launch_gemm_down(mh, md, offsets, d.E, R, d.H, d.I, y, status, g_wait_limit.load(),
@@ -236,9 +237,9 @@ moe_status do_shared_expert(const void* x, const void* packed, int T, int H, int
   const uint16_t* w2 = w1 + (size_t)G * 2 * Ig * H;
   MOE_CUDA(launch_uniform_offsets(offsets, G, T, s));
   const GemmOperand ma{x, (uint64_t)H, (uint64_t)T};
-  const GemmOperand mb{w1, (uint64_t)H, (uint64_t)G * 2 * Ig};
+  const GemmOperand mb{w1, 64, (uint64_t)G * 2 * Ig * (H / 64)};
   const GemmOperand mh{h, (uint64_t)Ig, (uint64_t)R};
-  const GemmOperand md{w2, (uint64_t)Ig, (uint64_t)G * H};
+  const GemmOperand md{w2, 64, (uint64_t)G * H * (Ig / 64)};
   MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, G, R, H, Ig, h, status, g_wait_limit.load(), s,
                                true));
   MOE_CUDA(launch_gemm_down(mh, md, offsets, G, R, H, Ig, shared_out, status, g_wait_limit.load(),
