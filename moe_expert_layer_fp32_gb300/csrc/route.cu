@@ -19,10 +19,11 @@
 // earlier chunks are multiplied (four CTAs fit on an SM); x is widened once to FP32 into a transposed
 // buffer, so a warp's eight token values for one h are two broadcast loads.
 //
-// route_small_kernel (T small): one CTA = 1, 2, 4 or 8 tokens; thread (g, e) owns
-// expert e for a group of the CTA's tokens; W_r and x stream through a six-stage
-// cp.async ring of 16 KB W_r chunks (about 100 KB in flight), since with few
-// CTAs the K loop is bound by how much of W_r each one keeps in flight.
+// route_cluster_kernel (T <= 64): a cluster of eight CTAs per 1, 2, 4 or 8
+// tokens, each CTA owning an eighth of the experts and streaming only those
+// columns of W_r; logits meet in the first CTA's shared memory (see below).
+//
+// route_tile_kernel (256 experts, large T): 2D warp tiles (see below).
 //
 // Epilogue (shared): logits go to shared memory; one warp per token runs k
 // rounds of a warp-wide argmax under the key (logit desc, expert asc), then the
@@ -487,57 +488,72 @@ __global__ void __launch_bounds__(NTHR, 4) route_tile_kernel(const uint16_t* __r
   }
 }
 
-// ------------------------------------------------------------- small T ---
-constexpr int SNST = 6;    // ring depth: ~100 KB of W_r in flight per CTA
+// ------------------------------------------------ small T, CTA clusters ---
+// route_cluster_kernel: a cluster of kCC CTAs routes TSV tokens; CTA r owns the
+// EC = EP / kCC experts [r*EC, (r+1)*EC) and streams only those columns of W_r
+// (EC*4 contiguous bytes per hidden row), so kCC SMs share the weight traffic that
+// one CTA carried alone.  Thread (tok, el) runs the FMA chain of token tok and
+// expert r*EC + el over h = 0..H-1 (the same chain as the other router kernels),
+// reading W_r and x from a cp.async ring.  The logits go into the first CTA's
+// shared memory (distributed shared memory), and after a cluster barrier its warps
+// run the shared per-token epilogue.
+constexpr int kCC = 8;       // CTAs per cluster
 
 template <int EP, int TSV>
-struct SmallCfg {
-  static constexpr int HC = 4096 / EP;                       // 16 KB of W_r per stage
-  static constexpr int TL = (TSV < 256 / EP) ? TSV : 256 / EP;  // token groups
-  static constexpr int TPT = TSV / TL;                       // tokens per thread
-  static constexpr int NTH = EP * TL;                        // threads
-  static constexpr int ring = SNST * (HC * EP * 4 + TSV * HC * 2);
-  static constexpr int bytes = ring + HC * TSV * 4;           // + FP32 x of one chunk
+struct ClusterCfg {
+  static constexpr int EC = EP / kCC;                  // experts per CTA
+  static constexpr int HC = (EP >= 256) ? 64 : 128;    // hidden rows per stage (divides H)
+  static constexpr int CNST = (EP <= 64) ? 12 : 6;     // ring depth: 24-48 KB of W_r in flight
+  static constexpr int NCMP = EC * TSV;                // computing threads
+  static constexpr int NTH = NCMP < 128 ? 128 : NCMP;  // all of them copy
+  static constexpr int LLD = EP + 1;
+  static constexpr int ring = CNST * (HC * EC * 4 + TSV * HC * 2);
+  static constexpr int bytes = ring + TSV * LLD * 4;
 };
 
-// TSV tokens per CTA (1, 2, 4 or 8): thread (g, e) owns expert e for the TPT
-// tokens g*TPT .. g*TPT+TPT-1 of the CTA.
 template <int EP, int TSV, int KIND>
-__global__ void __launch_bounds__(SmallCfg<EP, TSV>::NTH) route_small_kernel(
-    const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
-    int T, int H, int E, int k, int wbf16, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w) {
-  using C = SmallCfg<EP, TSV>;
-  constexpr int HC = C::HC, TPT = C::TPT, NTH = C::NTH;
+__global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(ClusterCfg<EP, TSV>::NTH)
+    route_cluster_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                         const float* __restrict__ bias, int T, int H, int E, int k, int wbf16,
+                         int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  using C = ClusterCfg<EP, TSV>;
+  constexpr int EC = C::EC, HC = C::HC, NTH = C::NTH, LLD = C::LLD, CNST = C::CNST;
   extern __shared__ float4 smem_f4[];
-  float* ws = reinterpret_cast<float*>(smem_f4);                    // [SNST][HC][EP]
-  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + SNST * HC * EP); // [SNST][TSV][HC]
-  float* xs = reinterpret_cast<float*>(xst + SNST * TSV * HC);      // [HC][TSV] FP32
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int e = tid % EP, g = tid / EP;
-  const int t0 = blockIdx.x * TSV;
+  float* ws = reinterpret_cast<float*>(smem_f4);                   // [CNST][HC][EC]
+  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + CNST * HC * EC); // [CNST][TSV][HC]
+  float* ls = reinterpret_cast<float*>(xst + CNST * TSV * HC);      // [TSV][LLD], CTA 0's used
+  const int tid = threadIdx.x;
+  const int rank = (int)cluster_ctarank();
+  const int e0 = rank * EC;                  // this CTA's first expert
+  const int t0 = (blockIdx.x / kCC) * TSV;   // the cluster's first token
   const int nchunks = H / HC;
+  const int ecols = max(0, min(EC, E - e0));  // valid experts of this CTA
 
-  if (E < EP) {
-    for (int i = tid; i < SNST * HC * EP; i += NTH)
-      if ((i % EP) >= E) ws[i] = 0.0f;
+  if (ecols < EC) {  // experts past E read zeros for the whole kernel
+    for (int i = tid; i < CNST * HC * EC; i += NTH)
+      if ((i % EC) >= ecols) ws[i] = 0.0f;
   }
   auto issue_chunk = [&](int c) {
     if (c < nchunks) {
-      const int buf = c % SNST;
+      const int buf = c % CNST;
       const int h0 = c * HC;
-      float* wdst = ws + buf * HC * EP;
-      const float* wsrc = wr + (size_t)h0 * E;
-      if (E == EP) {
-        for (int i = tid; i < HC * EP / 4; i += NTH) cp_async_16(wdst + 4 * i, wsrc + 4 * i, 16);
+      float* wdst = ws + buf * HC * EC;
+      if (ecols == EC && (E % 4) == 0) {
+        constexpr int PPR = EC / 4;  // 16-byte pieces per hidden row
+        for (int i = tid; i < HC * PPR; i += NTH) {
+          const int r = i / PPR, pc = i % PPR;
+          cp_async_16(wdst + r * EC + 4 * pc, wr + (size_t)(h0 + r) * E + e0 + 4 * pc, 16);
+        }
       } else {
-        for (int i = tid; i < HC * E; i += NTH)
-          cp_async_4(wdst + (i / E) * EP + (i % E), wsrc + i);
+        for (int i = tid; i < HC * ecols; i += NTH) {
+          const int r = i / ecols, c2 = i % ecols;
+          cp_async_4(wdst + r * EC + c2, wr + (size_t)(h0 + r) * E + e0 + c2);
+        }
       }
-      constexpr int PPR = HC / 8;  // 16-byte pieces per x row
+      constexpr int XPR = HC / 8;  // 16-byte pieces per x row
       uint16_t* xdst = xst + buf * TSV * HC;
-      for (int i = tid; i < TSV * PPR; i += NTH) {
-        const int r = i / PPR, pc = i % PPR;
+      for (int i = tid; i < TSV * XPR; i += NTH) {
+        const int r = i / XPR, pc = i % XPR;
         const int t = t0 + r;
         const uint16_t* src = (t < T) ? x + (size_t)t * H + h0 + 8 * pc : x;
         cp_async_16(xdst + r * HC + 8 * pc, src, (t < T) ? 16 : 0);
@@ -546,82 +562,59 @@ __global__ void __launch_bounds__(SmallCfg<EP, TSV>::NTH) route_small_kernel(
     cp_async_commit();
   };
 
-  float acc[TPT];
+  const int el = tid % EC, tok = tid / EC;  // computing threads: tid < NCMP
+  float acc = 0.0f;
 #pragma unroll
-  for (int i = 0; i < TPT; ++i) acc[i] = 0.0f;
-#pragma unroll
-  for (int c = 0; c < SNST - 1; ++c) issue_chunk(c);
+  for (int c = 0; c < CNST - 1; ++c) issue_chunk(c);
   for (int c = 0; c < nchunks; ++c) {
-    const int buf = c % SNST;
-    issue_chunk(c + SNST - 1);
-    cp_async_wait<SNST - 1>();
+    const int buf = c % CNST;
+    issue_chunk(c + CNST - 1);
+    cp_async_wait<CNST - 1>();
     __syncthreads();
-    // x chunk widened to FP32, transposed: xs[h][token], a thread's tokens adjacent
-    const uint16_t* xsb = xst + buf * TSV * HC;
-    for (int i = tid; i < TSV * HC; i += NTH) {
-      const int r = i / HC, hh = i % HC;
-      xs[hh * TSV + r] = __uint_as_float((uint32_t)xsb[r * HC + hh] << 16);
-    }
-    __syncthreads();
-    const float* wsb = ws + buf * HC * EP;
-#pragma unroll 8
-    for (int hh = 0; hh < HC; ++hh) {
-      const float wv = wsb[hh * EP + e];
-      float xv[TPT];
-      if constexpr (TPT % 4 == 0) {
-#pragma unroll
-        for (int q = 0; q < TPT / 4; ++q) {
-          const float4 v = *reinterpret_cast<const float4*>(xs + hh * TSV + g * TPT + 4 * q);
-          xv[4 * q] = v.x;
-          xv[4 * q + 1] = v.y;
-          xv[4 * q + 2] = v.z;
-          xv[4 * q + 3] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < TPT; ++i) xv[i] = xs[hh * TSV + g * TPT + i];
-      }
-#pragma unroll
-      for (int i = 0; i < TPT; ++i) acc[i] = fmaf(xv[i], wv, acc[i]);
+    if (tid < C::NCMP) {
+      const float* wsb = ws + buf * HC * EC + el;
+      const uint16_t* xsb = xst + buf * TSV * HC + tok * HC;
+#pragma unroll 16
+      for (int hh = 0; hh < HC; ++hh)
+        acc = fmaf(__uint_as_float((uint32_t)xsb[hh] << 16), wsb[hh * EC], acc);
     }
     __syncthreads();
   }
   cp_async_wait<0>();
-  constexpr int LLD = EP + 1;
-  float* ls = ws;  // [TSV][LLD], over the drained ring
-  const bool add_bias = KIND == 0 && bias != nullptr;
-  if (e < E) {
-    const float b = add_bias ? __ldg(bias + e) : 0.0f;
-#pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-      float l = acc[i];
-      if (add_bias) l = __fadd_rn(l, b);
-      ls[(g * TPT + i) * LLD + e] = l;
-    }
+  // logits (+ bias for the softmax router) into CTA 0's shared memory
+  if (tid < C::NCMP && el < ecols) {
+    const int e = e0 + el;
+    float l = acc;
+    if (KIND == 0 && bias != nullptr) l = __fadd_rn(l, __ldg(bias + e));
+    const uint32_t dst = mapa_shared(smem_u32(ls + tok * LLD + e), 0);
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(l) : "memory");
   }
-  __syncthreads();
-  for (int tl = warp; tl < TSV; tl += NTH / 32) {
-    const int t = t0 + tl;
-    if (t < T)
-      route_one_token<EP, KIND>(ls + tl * LLD, KIND == 1 ? bias : nullptr, E, k, wbf16, lane, t,
-                                topk_idx, topk_w);
+  cluster_sync();
+  if (rank == 0) {
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int tl = warp; tl < TSV; tl += NTH / 32) {
+      const int t = t0 + tl;
+      if (t < T)
+        route_one_token<EP, KIND>(ls + tl * LLD, KIND == 1 ? bias : nullptr, E, k, wbf16, lane,
+                                  t, topk_idx, topk_w);
+    }
   }
 }
 
 template <int EP, int TSV, int KIND>
-cudaError_t launch_small(const void* x, const float* wr, const float* bias, int T, int H, int E,
-                         int k, int wbf16, int32_t* idx, float* w, cudaStream_t s) {
-  using C = SmallCfg<EP, TSV>;
+cudaError_t launch_cluster(const void* x, const float* wr, const float* bias, int T, int H, int E,
+                           int k, int wbf16, int32_t* idx, float* w, cudaStream_t s) {
+  using C = ClusterCfg<EP, TSV>;
   static bool attr[64] = {};
   int dv = 0;
   cudaGetDevice(&dv);
   if (dv < 64 && !attr[dv]) {
-    cudaError_t e = cudaFuncSetAttribute(route_small_kernel<EP, TSV, KIND>,
+    cudaError_t e = cudaFuncSetAttribute(route_cluster_kernel<EP, TSV, KIND>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::bytes);
     if (e != cudaSuccess) return e;
     attr[dv] = true;
   }
-  route_small_kernel<EP, TSV, KIND><<<(T + TSV - 1) / TSV, C::NTH, C::bytes, s>>>(
+  route_cluster_kernel<EP, TSV, KIND><<<kCC * ((T + TSV - 1) / TSV), C::NTH, C::bytes, s>>>(
       static_cast<const uint16_t*>(x), wr, bias, T, H, E, k, wbf16, idx, w);
   return cudaGetLastError();
 }
@@ -630,10 +623,10 @@ template <int EP, int KIND>
 cudaError_t launch_ep(const void* x, const float* wr, const float* bias, int T, int H, int E, int k,
                       int wbf16, int32_t* idx, float* w, cudaStream_t s) {
   if (T <= kRouteSmallMaxT) {
-    if (T == 1) return launch_small<EP, 1, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
-    if (T == 2) return launch_small<EP, 2, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
-    if (T <= 4) return launch_small<EP, 4, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
-    return launch_small<EP, 8, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    if (T == 1) return launch_cluster<EP, 1, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    if (T == 2) return launch_cluster<EP, 2, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    if (T <= 4) return launch_cluster<EP, 4, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    return launch_cluster<EP, 8, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
   }
   if constexpr (EP == 256) {
     // 2D tiles once T gives every SM at least one CTA.  Measured on GB300: 5% faster

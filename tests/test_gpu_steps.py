@@ -126,14 +126,14 @@ def test_combine(moe, case):
 
 
 def test_route_kernels_agree_bitwise(moe):
-    """With 256 experts the router switches to 2D-tiled CTAs once every SM gets
-    one (T >= 32 x SMs, 4864 on 152 SMs); every logit is the same FMA chain in
-    both kernels, so a token's experts and weights must be the same bits either
-    side of the switch."""
+    """Three router kernels: CTA clusters up to 64 tokens, 1D tiles, and (256
+    experts) 2D tiles once every SM gets a CTA (T >= 32 x SMs, 4864 on 152 SMs).
+    Every logit is the same FMA chain in all of them, so a token's experts and
+    weights must be the same bits whichever kernel ran."""
     wl = synth.WORKLOADS["large"]
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    Ts = (32 * sms - 1, 32 * sms + 96)
-    x = synth.tokens(wl, Ts[1])
+    Ts = (5, 64, 65, 32 * sms - 1, 32 * sms + 96)
+    x = synth.tokens(wl, Ts[-1])
     wr, bias = synth.router(wl)
     got = []
     for T in Ts:
@@ -142,6 +142,7 @@ def test_route_kernels_agree_bitwise(moe):
         w = torch.empty((T, wl.k), dtype=torch.float32, device="cuda")
         moe.moe_route(dev_bf16(x[:T]), dev(wr), None if bias is None else dev(bias), d, idx, w)
         got.append((idx.cpu().numpy(), w.cpu().numpy()))
-    n = Ts[0]
-    np.testing.assert_array_equal(got[0][0], got[1][0][:n])
-    np.testing.assert_array_equal(got[0][1].view(np.uint32), got[1][1][:n].view(np.uint32))
+    big_idx, big_w = got[-1]
+    for T, (idx, w) in zip(Ts[:-1], got[:-1]):
+        np.testing.assert_array_equal(idx, big_idx[:T])
+        np.testing.assert_array_equal(w.view(np.uint32), big_w[:T].view(np.uint32))
