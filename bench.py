@@ -43,7 +43,7 @@ METRIC = "routed tokens/s per MoE layer fwd"
 # DRAM bytes per launch of the gate/up GEMM on the large workload, from one ncu
 # capture (profiles/gemm_dram_traffic_large.md), valid while the kernel sources
 # are unchanged since the capture.
-GEMM_TRAFFIC_LARGE = {"bytes": 11498740224 + 1068532480, "sources_sha256_16": "610544b9b8958474"}
+GEMM_TRAFFIC_LARGE = {"bytes": 11433122304 + 1070496000, "sources_sha256_16": "6d16852a79425318"}
 
 
 def gemm_sources_hash():
@@ -527,9 +527,10 @@ def run_ours(args):
         cpu = {"value": S * k / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"first {S} of {T} tokens ({S * k} routed rows), {t:.1f} s"}
 
-    # route 1, dispatch 4 (2 up to 256 tokens: one ranking block), gate/up 1, down 1,
-    # combine 1; the shared expert adds its offsets fill and two GEMMs
-    launches_per_step = 1 + (2 if T <= 256 else 4) + 2 + 1
+    # route 1, dispatch 4 (1 up to 256 tokens: one ranking block, rows copied in the
+    # same launch), gate/up 1, down 1, combine 1; the shared expert adds its offsets
+    # fill and two GEMMs
+    launches_per_step = 1 + (1 if T <= 256 else 4) + 2 + 1
     if shard is not None and shard.Is:
         launches_per_step += 3
     if rank == 0:

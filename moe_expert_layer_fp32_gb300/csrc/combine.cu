@@ -11,15 +11,20 @@
 // each weight once in FP32 before the chain; a scale of 1 leaves the weights, and
 // so the result, unchanged.
 //
-// Memory-bound gather: one CTA per token, 16-byte loads of the k FP32 rows
-// (all issued before the FMA chain), 8-byte stores of four bf16 outputs.
+// Memory-bound gather: one CTA per token and column block, 16-byte loads of the k
+// FP32 rows (all issued before the FMA chain), 8-byte stores of four bf16 outputs.
+// Column blocks are split across CTAs (gridDim.y) when T alone would leave SMs
+// idle; every element's chain is the same either way.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace moe {
 namespace {
 
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ y,
+// SPLIT: gridDim.y CTAs share a token's columns.  That form is held to the
+// unsplit kernel's register count (five CTAs per SM) by its launch bound.
+template <bool SPLIT>
+__global__ void __launch_bounds__(128, SPLIT ? 5 : 0) combine_kernel(const float* __restrict__ y,
                                                       const float* __restrict__ topk_w,
                                                       const int32_t* __restrict__ row_of_slot,
                                                       int T, int H, int k, float scale,
@@ -41,11 +46,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     row[j] = (j < k) ? s_row[j] : -1;
     w[j] = (j < k) ? s_w[j] : 0.0f;
   }
-  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+  // this CTA's column block (a multiple of 4 * blockDim.x columns)
+  const int cols = SPLIT ? H / gridDim.y : H;
+  const int cb = SPLIT ? blockIdx.y * cols : 0;
+  const float* yb = y + cb;
+  for (int c = threadIdx.x * 4; c < cols; c += blockDim.x * 4) {
     float4 v[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j)
-      if (row[j] >= 0) v[j] = __ldg(reinterpret_cast<const float4*>(y + (size_t)row[j] * H + c));
+      if (row[j] >= 0) v[j] = __ldg(reinterpret_cast<const float4*>(yb + (size_t)row[j] * H + c));
     float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
@@ -59,7 +68,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     uint2 o;
     o.x = pack_bf16x2(a0, a1);
     o.y = pack_bf16x2(a2, a3);
-    *reinterpret_cast<uint2*>(out + (size_t)t * H + c) = o;
+    // (the output address is formed here: a pointer hoisted out of the loop
+    // costs about 40 registers and two CTAs per SM)
+    *reinterpret_cast<uint2*>(out + (size_t)t * H + cb + c) = o;
   }
 }
 
@@ -68,8 +79,18 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, int T,
                            int H, int k, float scale, void* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<T, 128, 0, s>>>(y, topk_w, row_of_slot, T, H, k, scale,
-                                   static_cast<uint16_t*>(out));
+  // split the columns of each token over up to H / 512 CTAs while the grid stays
+  // within four CTAs per SM (one wave)
+  int split = 1;
+  while (split * 2 <= H / 512 && H % (split * 2 * 512) == 0 &&
+         (long long)T * split * 2 <= 4LL * device_sm_count())
+    split *= 2;
+  if (split > 1)
+    combine_kernel<true><<<dim3(T, split), 128, 0, s>>>(y, topk_w, row_of_slot, T, H, k, scale,
+                                                        static_cast<uint16_t*>(out));
+  else
+    combine_kernel<false><<<T, 128, 0, s>>>(y, topk_w, row_of_slot, T, H, k, scale,
+                                            static_cast<uint16_t*>(out));
   return cudaGetLastError();
 }
 

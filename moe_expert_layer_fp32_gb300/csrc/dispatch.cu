@@ -164,20 +164,25 @@ __global__ void __launch_bounds__(PB) rank_kernel(const int32_t* __restrict__ to
   }
 }
 
-// T <= 256 (a single ranking block): masks, counts, offsets and stable ranks in
-// one CTA, the work of block_counts + scan + rank without two launches.
+// T <= 256 (a single ranking block): masks, counts, offsets, stable ranks and the
+// row copy in one launch, the work of block_counts + scan + rank + copy_rows.
+// ceil(T / 8) CTAs each rank all T tokens (at most 256 x k ids, from L2) and
+// then copy 8 of them, one warp per token; CTA 0 writes counts and offsets.
 __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __restrict__ topk_idx,
                                                             int T, int k, int E,
+                                                            const uint16_t* __restrict__ x, int H,
                                                             int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets,
                                                             int32_t* __restrict__ row_of_slot,
                                                             int32_t* __restrict__ slot_of_row,
+                                                            uint16_t* __restrict__ x_perm,
                                                             int32_t* status) {
   extern __shared__ uint32_t smem_u[];
   uint32_t* masks = smem_u;
   int32_t* sidx = reinterpret_cast<int32_t*>(smem_u + 8 * E);
   __shared__ int s_scan[kMaxE];
-  build_masks(topk_idx, T, k, E, 0, masks, sidx, status);
+  // every CTA ranks the whole (single) block; each then copies its own 8 tokens
+  build_masks(topk_idx, T, k, E, 0, masks, sidx, blockIdx.x == 0 ? status : nullptr);
   const int tid = threadIdx.x;
   int c = 0;
   if (tid < E) {
@@ -193,29 +198,56 @@ __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __res
     __syncthreads();
   }
   const int excl = s_scan[tid] - c;
-  if (tid < E) {
-    counts[tid] = c;
-    offsets[tid] = excl;
+  if (blockIdx.x == 0) {
+    if (tid < E) {
+      counts[tid] = c;
+      offsets[tid] = excl;
+    }
+    if (tid == 0) offsets[E] = s_scan[kMaxE - 1];
   }
-  if (tid == 0) offsets[E] = s_scan[kMaxE - 1];
   __syncthreads();
   s_scan[tid] = excl;  // first row of each expert
   __syncthreads();
-  const int lane = tid & 31, warp = tid >> 5;
-  if (tid >= T) return;
-  const uint32_t below = (1u << lane) - 1u;
-  for (int j = 0; j < k; ++j) {
-    const int e = sidx[tid * k + j];
-    const size_t s = (size_t)tid * k + j;
-    if (e < 0 || e >= E) {
-      row_of_slot[s] = -1;
-      continue;
+  const int lane = tid & 31;
+  const int t = blockIdx.x * 8 + (tid >> 5);  // this warp's token
+  if (t >= T) return;
+  const long long R = (long long)T * k;
+  // lane j < k ranks slot (t, j): the token sits in mask word t / 32, bit t % 32
+  int my_row = -1;
+  if (lane < k) {
+    const int e = sidx[t * k + lane];
+    const size_t sl = (size_t)t * k + lane;
+    if (e >= 0 && e < E) {
+      const int tw = t >> 5;
+      int rank = __popc(masks[tw * E + e] & ((1u << (t & 31)) - 1u));
+      for (int w = 0; w < tw; ++w) rank += __popc(masks[w * E + e]);
+      const long long row = (long long)s_scan[e] + rank;
+      if (row >= 0 && row < R) my_row = (int)row;
+      else flag_error(status, MOE_ERR_DEVICE_CHECK);
     }
-    int rank = __popc(masks[warp * E + e] & below);
-    for (int w = 0; w < warp; ++w) rank += __popc(masks[w * E + e]);
-    const int row = s_scan[e] + rank;
-    row_of_slot[s] = row;
-    slot_of_row[row] = (int32_t)s;
+    row_of_slot[sl] = my_row;
+    if (my_row >= 0) slot_of_row[my_row] = (int32_t)sl;
+  }
+  const int nv = H / 8;  // 16-byte vectors per row
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  constexpr int U = 8;
+  for (int c0 = 0; c0 < nv; c0 += 32 * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int cc = c0 + u * 32 + lane;
+      if (cc < nv) v[u] = __ldg(src + cc);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xFFFFFFFFu, my_row, j);
+      if (r < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * H);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int cc = c0 + u * 32 + lane;
+        if (cc < nv) dst[cc] = v[u];
+      }
+    }
   }
 }
 
@@ -327,11 +359,14 @@ cudaError_t launch_weighted_counts(const int32_t* topk_idx, const int32_t* q, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, int32_t* counts,
-                                  int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,
-                                  int32_t* status, cudaStream_t s) {
-  dispatch_small_kernel<<<1, PB, mask_smem_bytes(E, k), s>>>(topk_idx, T, k, E, counts, offsets,
-                                                             row_of_slot, slot_of_row, status);
+cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, const void* x,
+                                  int H, int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
+                                  int32_t* slot_of_row, void* x_perm, int32_t* status,
+                                  cudaStream_t s) {
+  const int nb = T > 0 ? (T + 7) / 8 : 1;
+  dispatch_small_kernel<<<nb, PB, mask_smem_bytes(E, k), s>>>(
+      topk_idx, T, k, E, static_cast<const uint16_t*>(x), H, counts, offsets, row_of_slot,
+      slot_of_row, static_cast<uint16_t*>(x_perm), status);
   return cudaGetLastError();
 }
 

@@ -45,10 +45,12 @@ cudaError_t launch_weighted_counts(const int32_t* topk_idx, const int32_t* q, in
 // offsets[g] = g * T for g = 0..G (G groups of T rows each)
 cudaError_t launch_uniform_offsets(int32_t* offsets, int G, int T, cudaStream_t s);
 
-// T <= kPermBlock: counts, offsets, row_of_slot and slot_of_row in one launch
-cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, int32_t* counts,
-                                  int32_t* offsets, int32_t* row_of_slot, int32_t* slot_of_row,
-                                  int32_t* status, cudaStream_t s);
+// T <= kPermBlock: counts, offsets, row_of_slot, slot_of_row and the permuted
+// rows x_perm in one launch
+cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, const void* x,
+                                  int H, int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
+                                  int32_t* slot_of_row, void* x_perm, int32_t* status,
+                                  cudaStream_t s);
 
 // x_perm[row_of_slot[t*k+j]] = x[t]
 cudaError_t launch_copy_rows(const void* x, const int32_t* row_of_slot, int T, int H, int k,

@@ -316,11 +316,11 @@ moe_status layer_fwd(const void* x, const float* w_router, const float* bias,
                         w, s));
   MOE_TRY(mark(1));
   if (d.T > 0 && d.T <= kPermBlock) {
-    // one ranking block: counts, offsets and ranks in a single launch
-    MOE_CUDA(launch_dispatch_small(idx, d.T, d.k, d.E, counts, offsets, ros, sor,
+    // one ranking block: counts, offsets, ranks and the row copy in a single
+    // launch (the load-statistics stage holds the permute; mark 2 closes both)
+    MOE_CUDA(launch_dispatch_small(idx, d.T, d.k, d.E, x, d.H, counts, offsets, ros, sor, x_perm,
                                    at<int32_t>(workspace, L.status), s));
     MOE_TRY(mark(2));
-    MOE_CUDA(launch_copy_rows(x, ros, d.T, d.H, d.k, x_perm, at<int32_t>(workspace, L.status), s));
   } else {
     MOE_TRY(do_load_stats(idx, d, counts, offsets, false, workspace, s));
     MOE_TRY(mark(2));
