@@ -227,6 +227,14 @@ moe_status moe_prepack_expert_weights_ex(const void* w_gate, const void* w_up,
 moe_status moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void* packed_weights,
                           moe_dims d, float* y, void* workspace, size_t ws_bytes, void* stream);
 
+/* Which form of the grouped GEMMs moe_expert_ffn (and every layer call) runs for
+ * these dims on the current device: 0 = tile kernels (128 token rows per MMA),
+ * 1 = swapped kernels (128 weight rows per MMA, up to 64 token rows on N; chosen
+ * while experts hold at most 8 rows on average and the gate/up work units number
+ * at most four per SM).  Both forms give the same bits for every row.
+ * Negative: minus a moe_status (invalid dims, no usable device). */
+int moe_expert_ffn_form(moe_dims d);
+
 /* Step: combine.  out[t, c] = bf16(acc), acc = 0, then for j = 0..k-1:
  *   acc = fmaf(topk_w[t,j], y[row_of_slot[t*k+j], c], acc).
  *   y [T*k, H] fp32; topk_w [T, k] fp32; row_of_slot [T*k] int32; out [T, H] bf16.

@@ -39,7 +39,7 @@ ABI_SYMBOLS = ("moe_workspace_bytes", "moe_packed_weight_bytes", "moe_route", "m
                "moe_tree_reduce_bf16", "moe_shared_packed_bytes", "moe_prepack_shared_expert",
                "moe_shared_expert_workspace_bytes", "moe_shared_expert",
                "moe_sharded_workspace_bytes", "moe_layer_fwd_sharded",
-               "moe_layer_fwd_sharded_profiled")
+               "moe_layer_fwd_sharded_profiled", "moe_expert_ffn_form")
 
 
 class moe_dims(ctypes.Structure):
@@ -104,6 +104,7 @@ _sig = {
                                            moe_dims, _vp, _vp, _vp]),
     "moe_tree_reduce_bf16": (ctypes.c_int, [_vp, _i32, ctypes.c_int64, _vp, _vp]),
     "moe_shared_packed_bytes": (_sz, [_i32, _i32]),
+    "moe_expert_ffn_form": (ctypes.c_int, [moe_dims]),
     "moe_prepack_shared_expert": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _sz, _vp]),
     "moe_shared_expert_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "moe_shared_expert": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
@@ -341,6 +342,14 @@ def moe_expert_ffn(x_perm, offsets, packed_weights, d, y, workspace, stream=None
     wp, wb = _ws(workspace)
     _check("moe_expert_ffn", _lib.moe_expert_ffn(_ptr(x_perm), _ptr(offsets), _ptr(packed_weights),
                                                  d, _ptr(y), wp, wb, _stream(stream)))
+
+
+def moe_expert_ffn_form(d):
+    """0: tile GEMMs, 1: swapped GEMMs (weight rows on the MMA's M side)."""
+    r = _lib.moe_expert_ffn_form(d)
+    if r < 0:
+        raise MoEError("moe_expert_ffn_form", -r)
+    return r
 
 
 def moe_combine(y, topk_w, row_of_slot, d, out, stream=None):

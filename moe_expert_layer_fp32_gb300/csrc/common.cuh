@@ -27,6 +27,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }
 
+// silu(g) = g / (1 + exp(-g)) on the special-function unit (ex2.approx, rcp.approx):
+// a few FP32 ulps from the correctly rounded value, which the one BF16 rounding of
+// h that follows mostly absorbs.  Both grouped GEMM kernels use this function, so
+// the same instructions run for every T.  The IEEE division and the library exp
+// made the SwiGLU epilogue about 21 us per 128 x 256 tile, longer than the main
+// loop for K = 2048.
+__device__ __forceinline__ float silu_f32(float g) {
+  return __fdividef(g, __fadd_rn(1.0f, __expf(-g)));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -100,6 +110,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
       return false;
     }
   }
+}
+
+// Wait for `parity` with a plain clock limit and no abort flag: used after an abort
+// to let a role's own copies or MMAs in flight finish before shared and tensor
+// memory are released.  Returns false if the limit ran out.
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long long limit) {
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > limit) return false;
+  return true;
 }
 
 // -------------------------------------------------------------------- TMA ---

@@ -140,22 +140,6 @@ __device__ __forceinline__ Work decode(int u, int rank, const int* s_prefix, con
   return w;
 }
 
-__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long long limit) {
-  long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > limit) return false;
-  return true;
-}
-
-// silu(g) = g / (1 + exp(-g)) on the special-function unit (ex2.approx, rcp.approx):
-// a few FP32 ulps from the correctly rounded value, which the one BF16 rounding of
-// h that follows mostly absorbs; the same instructions run for every T.  The IEEE
-// division and the library exp made the SwiGLU epilogue about 21 us per 128 x 256
-// tile, longer than the main loop for K = 2048.
-__device__ __forceinline__ float silu_f32(float g) {
-  return __fdividef(g, __fadd_rn(1.0f, __expf(-g)));
-}
-
 // One warp writes a 32-row x 128-byte block whose row i (i = lane) it holds in
 // registers: the rows go through shared memory so that every global store
 // instruction writes four whole 128-byte row segments instead of 32 scattered

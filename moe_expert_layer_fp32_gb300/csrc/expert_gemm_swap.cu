@@ -1,0 +1,369 @@
+// Grouped expert GEMMs for small batches: the weight rows on the MMA's M side.
+//
+// "RoutePack", section 2.3 (a rank's experts run as one grouped operation);
+// "0 train-infer mismatch for open-weight MoE RL", sections "SwiGLU: rounding
+// after the multiply" and "Matrix multiplication: the same reduction along K".
+// The same two GEMMs as the tile kernels in expert_gemm.cu:
+//   gate/up: h[r, :] = bf16(silu(x_perm[r] Wg_e) * (x_perm[r] Wu_e))
+//   down:    y[r, :] = h[r] Wd_e                              (FP32 out)
+//
+// When experts hold a handful of rows (decode), a 128-row token tile is almost
+// empty and each MMA of N = 256 weight columns costs the full tensor time for a
+// few useful rows.  Here the transposed product is formed instead:
+//   D^T[w, r] = sum_k W[w, k] X[r, k]
+// with M = 128 weight rows per MMA and N = 16, 32 or 64 token rows, so the MMAs
+// are short and the kernel is bound by streaming the weights from HBM.
+//
+// Work unit: (expert e, one packed 256-row weight box column, up to 64 of e's
+// rows).  The box's two 128-row halves are the two M = 128 operands: for gate/up
+// the gate and the up rows of the same 128 intermediate columns (the packed
+// interleave), for down two 128-column halves of the output.  Per stage the
+// producer loads one 256 x 64 weight box (32 KB, contiguous in the box-tiled
+// packing) and one N x 64 token box; the MMA issuer runs, per 16-wide K step,
+// one MMA per half into two TMEM accumulators of N columns (double-buffered).
+// Units are numbered expert-major, then weight column, then token tile, so the
+// token tiles of one weight column run side by side and share its L2 lines.
+//
+// Each output element is the same K order (64-wide k-blocks ascending, 16-wide
+// MMAs ascending, FP32 accumulation from zero) over the same BF16 products as in
+// the tile kernels, and the epilogue applies the same operations (silu_f32, one
+// FP32 product, one BF16 rounding; or the FP32 value as it is).  A layer test
+// checks that rows computed here and by the tile kernels are bit-identical, which
+// keeps the output batch-invariant when the host switches forms with the number
+// of rows.
+//
+// Roles and bounded waits are those of the tile kernels: warp 0 lane 0 TMA
+// producer, warp 1 lane 0 MMA issuer, warps 2..5 epilogue (TMEM lane quarter =
+// warp % 4); every wait has a clock limit and an abort path that drains this
+// CTA's own copies and MMAs before tensor memory is freed.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int SK = 64;                       // k-block: one 128-byte swizzle row
+constexpr int SUK = 16;                      // MMA K
+constexpr int WROWS = 256;                   // weight rows per unit (one packed box)
+constexpr int HALF = 128;                    // MMA M
+constexpr int TT = 64;                       // token rows per unit at most (MMA N <= 64)
+constexpr int STAGES = 5;
+constexpr int W_BYTES = WROWS * SK * 2;      // 32 KB
+constexpr int X_BYTES = TT * SK * 2;         // 8 KB (N = 64)
+constexpr int ACC_COLS = 2 * TT;             // one accumulator buffer: two halves of N <= 64
+constexpr int TMEM_COLS = 2 * ACC_COLS;      // double-buffered
+constexpr int NBAR = 2 * STAGES + 2 + 2 + 1;
+constexpr int SMEM_BYTES =
+    1024 + STAGES * (W_BYTES + X_BYTES) + NBAR * 8 + 16 + 3 * (kMaxE + 1) * 4;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+
+// Weight boxes (256 rows) and token boxes of 16, 32 and 64 rows; all 64 columns.
+struct SwapMaps {
+  CUtensorMap w, x16, x32, x64;
+};
+
+struct SwapWork {
+  int e, wt;       // expert, weight box column (256 output rows of the transposed tile)
+  int row0, rows;  // first token row (output row) and rows that belong to e (<= TT)
+  int nb;          // MMA N = token box rows: 16, 32 or 64
+  int x_load_row;  // first row of the token box
+  int w_load_row;  // box row of k-block 0 in the packed weights
+};
+
+__device__ __forceinline__ SwapWork swap_decode(int u, const int* s_prefix, const int* s_off,
+                                                const int* s_tt, int E, int NTW, int KB,
+                                                int a_local) {
+  // largest e with s_prefix[e] <= u (experts without rows share the next prefix)
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_prefix[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  const int local = u - s_prefix[lo];
+  const int tt = s_tt[lo];
+  SwapWork w;
+  w.e = lo;
+  w.wt = local / tt;
+  const int ti = local - w.wt * tt;
+  w.row0 = s_off[lo] + ti * TT;
+  w.rows = min(TT, s_off[lo + 1] - w.row0);
+  w.nb = w.rows <= 16 ? 16 : (w.rows <= 32 ? 32 : 64);
+  w.x_load_row = w.row0 - (a_local ? s_off[lo] : 0);
+  w.w_load_row = (lo * NTW + w.wt) * KB * WROWS;
+  return w;
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(192, 1)
+    grouped_gemm_swap_kernel(const __grid_constant__ SwapMaps maps,
+                             const int32_t* __restrict__ offsets, int E, int R, int n_per_expert,
+                             int K, void* __restrict__ out, int out_ld, int32_t* status,
+                             long long spin_limit, int a_local) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sW = base;
+  uint8_t* sX = base + STAGES * W_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sX + STAGES * X_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_off = s_prefix + (kMaxE + 1);
+  int* s_tt = s_off + (kMaxE + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NTW = n_per_expert / WROWS;
+  const int KB = K / SK;
+
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = __ldg(offsets + e);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // schedule: validate offsets (0 = o_0 <= o_1 <= ... <= o_E = R), work prefix
+    bool ok = s_off[0] == 0 && s_off[E] == R;
+    int p = 0;
+    for (int e = 0; e < E; ++e) {
+      const int a = s_off[e], b = s_off[e + 1];
+      if (b < a) ok = false;
+      const int tt = b > a ? (b - a + TT - 1) / TT : 0;
+      s_tt[e] = tt;
+      s_prefix[e] = p;
+      p += tt * NTW;
+    }
+    if (!ok) {
+      flag_error(status, MOE_ERR_DEVICE_CHECK);
+      for (int e = 0; e < E; ++e) s_prefix[e] = 0;
+      p = 0;
+    }
+    s_prefix[E] = p;
+    *abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&maps.w);
+    prefetch_tensormap(&maps.x16);
+    prefetch_tensormap(&maps.x32);
+    prefetch_tensormap(&maps.x64);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = s_prefix[E];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int it = 0;
+      bool aborted = false;
+      for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
+        const SwapWork w = swap_decode(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
+        const CUtensorMap* xm = w.nb == 16 ? &maps.x16 : (w.nb == 32 ? &maps.x32 : &maps.x64);
+        const uint32_t bytes = W_BYTES + w.nb * SK * 2;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, status, spin_limit)) {
+            aborted = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+          tma_load_2d(&maps.w, sW + s * W_BYTES, &full[s], 0, w.w_load_row + kb * WROWS);
+          tma_load_2d(xm, sX + s * X_BYTES, &full[s], kb * SK, w.x_load_row);
+        }
+      }
+      if (aborted) {
+        for (int i = (it > STAGES ? it - STAGES : 0); i < it; ++i)
+          wait_drain(&full[i % STAGES], (i / STAGES) & 1, kSpinLimitCycles);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      int it = 0, tcount = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
+        const SwapWork w = swap_decode(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
+        const uint32_t idesc = idesc_bf16_f32(HALF, w.nb);
+        const int acc = tcount & 1;
+        const uint32_t aph = (tcount >> 1) & 1;
+        if (!mbar_wait_bounded(&tempty[acc], aph ^ 1, abort_flag, status, spin_limit)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + acc * ACC_COLS;  // half 0; half 1 at + TT
+        bool aborted = false;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait_bounded(&full[s], ph, abort_flag, status, spin_limit)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t w_addr = smem_u32(sW + s * W_BYTES);
+          const uint32_t x_addr = smem_u32(sX + s * X_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < SK / SUK; ++kk) {
+            const uint64_t xd = sdesc_k_major_sw128(x_addr + kk * SUK * 2);
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            mma_bf16(d0, sdesc_k_major_sw128(w_addr + kk * SUK * 2), xd, idesc, accum);
+            mma_bf16(d0 + TT, sdesc_k_major_sw128(w_addr + HALF * 128 + kk * SUK * 2), xd, idesc,
+                     accum);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (aborted) break;
+        mma_commit(&tfull[acc]);
+      }
+      mma_commit(mma_done);
+      wait_drain(mma_done, 0, kSpinLimitCycles);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    // TMEM lane (32 q + lane) = weight row of each half; column j = token row0 + j.
+    const int q = warp & 3;
+    int tcount = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
+      const SwapWork w = swap_decode(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
+      const int acc = tcount & 1;
+      const uint32_t aph = (tcount >> 1) & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(&tfull[acc], aph, abort_flag, status, spin_limit);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+      if constexpr (SWIGLU) {
+        // half 0: gate, half 1: up, of intermediate column wt * 128 + 32 q + lane
+        uint16_t* h = static_cast<uint16_t*>(out) + (size_t)w.wt * HALF + q * 32 + lane;
+        for (int j0 = 0; j0 < w.nb; j0 += 16) {
+          uint32_t g[16], uu[16];
+          tmem_ld_32x32b_x16(taddr + j0, g);
+          tmem_ld_32x32b_x16(taddr + TT + j0, uu);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = j0 + i;
+            if (j < w.rows) {
+              const float hv =
+                  __fmul_rn(silu_f32(__uint_as_float(g[i])), __uint_as_float(uu[i]));
+              h[(size_t)(w.row0 + j) * out_ld] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+            }
+          }
+        }
+      } else {
+        // half c: output columns wt * 256 + 128 c + 32 q + lane
+        float* y = static_cast<float*>(out) + (size_t)w.wt * WROWS + q * 32 + lane;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          for (int j0 = 0; j0 < w.nb; j0 += 16) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(taddr + c * TT + j0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = j0 + i;
+              if (j < w.rows) y[(size_t)(w.row0 + j) * out_ld + c * HALF] = __uint_as_float(v[i]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <bool SWIGLU>
+cudaError_t launch_swap(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets, int E,
+                        int R, int n_per_expert, int K, void* out, int out_ld, int32_t* status,
+                        long long spin_limit, cudaStream_t s, int a_local) {
+  SwapMaps m;
+  if (!b.encode(&m.w, WROWS) || !a.encode(&m.x16, 16) || !a.encode(&m.x32, 32) ||
+      !a.encode(&m.x64, TT))
+    return cudaErrorInvalidValue;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 64 || !attr_set[dev]) {
+    err = cudaFuncSetAttribute(grouped_gemm_swap_kernel<SWIGLU>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  // units <= weight columns x (experts with rows + R / TT): one CTA per unit up to
+  // one per SM (the kernel is persistent beyond that)
+  const long long units =
+      (long long)(n_per_expert / WROWS) * (std::min<long long>(E, R) + R / TT);
+  const int grid = (int)std::max<long long>(1, std::min<long long>(device_sm_count(), units));
+  grouped_gemm_swap_kernel<SWIGLU><<<grid, 192, SMEM_BYTES, s>>>(
+      m, offsets, E, R, n_per_expert, K, out, out_ld, status, spin_limit, a_local);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Measured on GB300 (L2 flushed, CUDA graph): the swapped form is 2-10% faster for
+// fine_grained at T <= 64 and ling3_tiny at T <= 64, where the tile kernels' units
+// are few and bound by one SM's tensor time per 128-row tile.  It is 4% slower for
+// fine_grained at T >= 128 and for `large` at T = 64, where experts hold more rows
+// or the units run many waves and both forms stream the weights at the HBM rate.
+bool use_swap_gemm(int E, int R, int H, int I) {
+  if ((2 * I) % WROWS != 0 || H % WROWS != 0) return false;
+  if ((long long)R > (long long)kSwapRowsPerExpert * E) return false;
+  const long long units = (long long)(2 * I / WROWS) * std::min(E, R);
+  return units <= 4LL * device_sm_count();
+}
+
+cudaError_t launch_gemm_gate_up_swap(const GemmOperand& a, const GemmOperand& b,
+                                     const int32_t* offsets, int E, int R, int H, int I, void* h,
+                                     int32_t* status, long long spin_limit, cudaStream_t s,
+                                     bool a_local) {
+  if (R == 0) return cudaSuccess;
+  return launch_swap<true>(a, b, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
+                           a_local ? 1 : 0);
+}
+
+cudaError_t launch_gemm_down_swap(const GemmOperand& a, const GemmOperand& b,
+                                  const int32_t* offsets, int E, int R, int H, int I, float* y,
+                                  int32_t* status, long long spin_limit, cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  return launch_swap<false>(a, b, offsets, E, R, H, I, y, H, status, spin_limit, s, 0);
+}
+
+}  // namespace moe

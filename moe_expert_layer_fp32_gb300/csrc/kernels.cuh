@@ -14,6 +14,7 @@ constexpr int kMaxShards = 16;  // expert ranks of the sharded combine / tree
 constexpr int kPermBlock = 256;  // tokens per ranking block of the permutation
 constexpr long long kSpinLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int kRouteSmallMaxT = 64;  // batches up to this size use the small-T router kernel
+constexpr int kRouteClusterMaxT = 1024;  // and up to this size its eight-token clusters
 
 // router: projection (FP32 FMA chain), then kind 0: softmax, top-k (bias joins the
 // logits); kind 1: sigmoid scores, top-k on score + correction bias, weights from
@@ -92,6 +93,20 @@ cudaError_t launch_gemm_down(const GemmOperand& a, const GemmOperand& b,
 
 // N tile width of the down projection for this H (fixed per model shape)
 int gemm_down_bn(int H);
+
+// The same two GEMMs with the weight rows on the MMA's M side and up to 64 token
+// rows on N (small batches); outputs bit-identical to the tile kernels above.
+// use_swap_gemm: at most kSwapRowsPerExpert rows per expert on average and at
+// most four gate/up work units per SM (experts with rows <= min(E, R)).
+constexpr int kSwapRowsPerExpert = 8;
+bool use_swap_gemm(int E, int R, int H, int I);
+cudaError_t launch_gemm_gate_up_swap(const GemmOperand& a, const GemmOperand& b,
+                                     const int32_t* offsets, int E, int R, int H, int I, void* h,
+                                     int32_t* status, long long spin_limit, cudaStream_t s,
+                                     bool a_local = false);
+cudaError_t launch_gemm_down_swap(const GemmOperand& a, const GemmOperand& b,
+                                  const int32_t* offsets, int E, int R, int H, int I, float* y,
+                                  int32_t* status, long long spin_limit, cudaStream_t s);
 
 // out[t] = bf16(slot-order FMA chain of (scale * topk_w[t,j]) * y[row_of_slot[t*k+j]])
 cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, int T,

@@ -216,10 +216,18 @@ moe_status do_expert_ffn(const void* x_perm, const int32_t* offsets, const void*
   const GemmOperand mb{w1, 64, (uint64_t)d.E * 2 * d.I * (d.H / 64)};
   const GemmOperand mh{h, (uint64_t)d.I, (uint64_t)R};
   const GemmOperand md{w2, 64, (uint64_t)d.E * d.H * (d.I / 64)};
-  MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, d.E, R, d.H, d.I, h, status, g_wait_limit.load(), s));
+  // few rows per expert: weight rows on the MMA's M side (same bits as the tiles)
+  const bool swap = use_swap_gemm(d.E, R, d.H, d.I);
+  const long long lim = g_wait_limit.load();
+  if (swap)
+    MOE_CUDA(launch_gemm_gate_up_swap(ma, mb, offsets, d.E, R, d.H, d.I, h, status, lim, s));
+  else
+    MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, d.E, R, d.H, d.I, h, status, lim, s));
   if (after_gate_up != nullptr) MOE_CUDA(cudaEventRecord(after_gate_up, s));
-  MOE_CUDA(launch_gemm_down(mh, md, offsets, d.E, R, d.H, d.I, y, status, g_wait_limit.load(),
-                            s));
+  if (swap)
+    MOE_CUDA(launch_gemm_down_swap(mh, md, offsets, d.E, R, d.H, d.I, y, status, lim, s));
+  else
+    MOE_CUDA(launch_gemm_down(mh, md, offsets, d.E, R, d.H, d.I, y, status, lim, s));
   return MOE_OK;
 }
 
@@ -240,10 +248,14 @@ moe_status do_shared_expert(const void* x, const void* packed, int T, int H, int
   const GemmOperand mb{w1, 64, (uint64_t)G * 2 * Ig * (H / 64)};
   const GemmOperand mh{h, (uint64_t)Ig, (uint64_t)R};
   const GemmOperand md{w2, 64, (uint64_t)G * H * (Ig / 64)};
-  MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, G, R, H, Ig, h, status, g_wait_limit.load(), s,
-                               true));
-  MOE_CUDA(launch_gemm_down(mh, md, offsets, G, R, H, Ig, shared_out, status, g_wait_limit.load(),
-                            s));
+  const long long lim = g_wait_limit.load();
+  if (use_swap_gemm(G, R, H, Ig)) {
+    MOE_CUDA(launch_gemm_gate_up_swap(ma, mb, offsets, G, R, H, Ig, h, status, lim, s, true));
+    MOE_CUDA(launch_gemm_down_swap(mh, md, offsets, G, R, H, Ig, shared_out, status, lim, s));
+  } else {
+    MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, G, R, H, Ig, h, status, lim, s, true));
+    MOE_CUDA(launch_gemm_down(mh, md, offsets, G, R, H, Ig, shared_out, status, lim, s));
+  }
   return MOE_OK;
 }
 
@@ -591,6 +603,13 @@ moe_status moe_expert_ffn(const void* x_perm, const int32_t* offsets, const void
   MOE_TRY(need(y));
   MOE_TRY(device_ok());
   return do_expert_ffn(x_perm, offsets, packed_weights, d, y, workspace, as_stream(stream));
+}
+
+int moe_expert_ffn_form(moe_dims d) {
+  moe_status st = check_dims(d);
+  if (st == MOE_OK) st = device_ok();
+  if (st != MOE_OK) return -(int)st;
+  return use_swap_gemm(d.E, d.T * d.k, d.H, d.I) ? 1 : 0;
 }
 
 moe_status moe_combine_ex(const float* y, const float* topk_w, const int32_t* row_of_slot,

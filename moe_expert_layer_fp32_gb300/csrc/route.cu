@@ -19,7 +19,7 @@
 // earlier chunks are multiplied (four CTAs fit on an SM); x is widened once to FP32 into a transposed
 // buffer, so a warp's eight token values for one h are two broadcast loads.
 //
-// route_cluster_kernel (T <= 64): a cluster of eight CTAs per 1, 2, 4 or 8
+// route_cluster_kernel (T <= 1024): a cluster of eight CTAs per 1, 2, 4 or 8
 // tokens, each CTA owning an eighth of the experts and streaming only those
 // columns of W_r; logits meet in the first CTA's shared memory (see below).
 //
@@ -494,7 +494,10 @@ __global__ void __launch_bounds__(NTHR, 4) route_tile_kernel(const uint16_t* __r
 // (EC*4 contiguous bytes per hidden row), so kCC SMs share the weight traffic that
 // one CTA carried alone.  Thread (tok, el) runs the FMA chain of token tok and
 // expert r*EC + el over h = 0..H-1 (the same chain as the other router kernels),
-// reading W_r and x from a cp.async ring.  The logits go into the first CTA's
+// reading W_r and x from a cp.async ring.  The ring holds each W_r chunk
+// transposed (one padded row of HC hidden values per expert), so a thread reads
+// eight consecutive h with two 16-byte loads of W_r and one of x: at T = 1 the
+// kernel's time is this one dependent chain of H FMAs.  The logits go into the first CTA's
 // shared memory (distributed shared memory), and after a cluster barrier its warps
 // run the shared per-token epilogue.
 constexpr int kCC = 8;       // CTAs per cluster
@@ -503,11 +506,12 @@ template <int EP, int TSV>
 struct ClusterCfg {
   static constexpr int EC = EP / kCC;                  // experts per CTA
   static constexpr int HC = (EP >= 256) ? 64 : 128;    // hidden rows per stage (divides H)
+  static constexpr int HCP = HC + 4;                   // padded row of the transposed chunk
   static constexpr int CNST = (EP <= 64) ? 12 : 6;     // ring depth: 24-48 KB of W_r in flight
   static constexpr int NCMP = EC * TSV;                // computing threads
   static constexpr int NTH = NCMP < 128 ? 128 : NCMP;  // all of them copy
   static constexpr int LLD = EP + 1;
-  static constexpr int ring = CNST * (HC * EC * 4 + TSV * HC * 2);
+  static constexpr int ring = CNST * (EC * HCP * 4 + TSV * HC * 2);
   static constexpr int bytes = ring + TSV * LLD * 4;
 };
 
@@ -517,10 +521,11 @@ __global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(ClusterCfg<EP, TSV
                          const float* __restrict__ bias, int T, int H, int E, int k, int wbf16,
                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   using C = ClusterCfg<EP, TSV>;
-  constexpr int EC = C::EC, HC = C::HC, NTH = C::NTH, LLD = C::LLD, CNST = C::CNST;
+  constexpr int EC = C::EC, HC = C::HC, HCP = C::HCP, NTH = C::NTH, LLD = C::LLD,
+                CNST = C::CNST;
   extern __shared__ float4 smem_f4[];
-  float* ws = reinterpret_cast<float*>(smem_f4);                   // [CNST][HC][EC]
-  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + CNST * HC * EC); // [CNST][TSV][HC]
+  float* ws = reinterpret_cast<float*>(smem_f4);                    // [CNST][EC][HCP]
+  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + CNST * EC * HCP); // [CNST][TSV][HC]
   float* ls = reinterpret_cast<float*>(xst + CNST * TSV * HC);      // [TSV][LLD], CTA 0's used
   const int tid = threadIdx.x;
   const int rank = (int)cluster_ctarank();
@@ -530,24 +535,25 @@ __global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(ClusterCfg<EP, TSV
   const int ecols = max(0, min(EC, E - e0));  // valid experts of this CTA
 
   if (ecols < EC) {  // experts past E read zeros for the whole kernel
-    for (int i = tid; i < CNST * HC * EC; i += NTH)
-      if ((i % EC) >= ecols) ws[i] = 0.0f;
+    for (int i = tid; i < CNST * EC * HCP; i += NTH)
+      if ((i / HCP) % EC >= ecols) ws[i] = 0.0f;
   }
   auto issue_chunk = [&](int c) {
     if (c < nchunks) {
       const int buf = c % CNST;
       const int h0 = c * HC;
-      float* wdst = ws + buf * HC * EC;
-      if (ecols == EC && (E % 4) == 0) {
-        constexpr int PPR = EC / 4;  // 16-byte pieces per hidden row
-        for (int i = tid; i < HC * PPR; i += NTH) {
-          const int r = i / PPR, pc = i % PPR;
-          cp_async_16(wdst + r * EC + 4 * pc, wr + (size_t)(h0 + r) * E + e0 + 4 * pc, 16);
+      float* wdst = ws + buf * EC * HCP;
+      // consecutive threads read consecutive experts of one hidden row (coalesced)
+      // and write them transposed, one padded row per expert
+      if (ecols == EC) {
+        for (int i = tid; i < HC * EC; i += NTH) {
+          const int r = i / EC, c2 = i % EC;
+          cp_async_4(wdst + c2 * HCP + r, wr + (size_t)(h0 + r) * E + e0 + c2);
         }
       } else {
         for (int i = tid; i < HC * ecols; i += NTH) {
           const int r = i / ecols, c2 = i % ecols;
-          cp_async_4(wdst + r * EC + c2, wr + (size_t)(h0 + r) * E + e0 + c2);
+          cp_async_4(wdst + c2 * HCP + r, wr + (size_t)(h0 + r) * E + e0 + c2);
         }
       }
       constexpr int XPR = HC / 8;  // 16-byte pieces per x row
@@ -572,11 +578,22 @@ __global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(ClusterCfg<EP, TSV
     cp_async_wait<CNST - 1>();
     __syncthreads();
     if (tid < C::NCMP) {
-      const float* wsb = ws + buf * HC * EC + el;
+      const float* wsb = ws + buf * EC * HCP + el * HCP;
       const uint16_t* xsb = xst + buf * TSV * HC + tok * HC;
-#pragma unroll 16
-      for (int hh = 0; hh < HC; ++hh)
-        acc = fmaf(__uint_as_float((uint32_t)xsb[hh] << 16), wsb[hh * EC], acc);
+#pragma unroll 4
+      for (int hh = 0; hh < HC; hh += 8) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xsb + hh);
+        const float4 w0 = *reinterpret_cast<const float4*>(wsb + hh);
+        const float4 w1 = *reinterpret_cast<const float4*>(wsb + hh + 4);
+        acc = fmaf(bf16_lo(xv.x), w0.x, acc);
+        acc = fmaf(bf16_hi(xv.x), w0.y, acc);
+        acc = fmaf(bf16_lo(xv.y), w0.z, acc);
+        acc = fmaf(bf16_hi(xv.y), w0.w, acc);
+        acc = fmaf(bf16_lo(xv.z), w1.x, acc);
+        acc = fmaf(bf16_hi(xv.z), w1.y, acc);
+        acc = fmaf(bf16_lo(xv.w), w1.z, acc);
+        acc = fmaf(bf16_hi(xv.w), w1.w, acc);
+      }
     }
     __syncthreads();
   }
@@ -628,6 +645,13 @@ cudaError_t launch_ep(const void* x, const float* wr, const float* bias, int T, 
     if (T <= 4) return launch_cluster<EP, 4, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
     return launch_cluster<EP, 8, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
   }
+  // Clusters of eight tokens up to kRouteClusterMaxT.  Measured on GB300 (router
+  // stage, L2 flushed): fine_grained T = 128 / 512: 27 / 49 us against 77 / 78 us
+  // for route_kernel; large T = 256: 84 against 314 us.  From about 1000 tokens
+  // route_kernel (all experts of 32 tokens per CTA) is faster: fine_grained
+  // T = 2048: 79 against 137 us; large T = 2048: 321 against 537 us.
+  if (T <= kRouteClusterMaxT)
+    return launch_cluster<EP, 8, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
   if constexpr (EP == 256) {
     // 2D tiles once T gives every SM at least one CTA.  Measured on GB300: 5% faster
     // than route_kernel for 256 experts; for 64 and 128 experts (fewer experts per

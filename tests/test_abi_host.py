@@ -67,6 +67,9 @@ def test_bad_dims_rejected_before_launch(moe, T, H, E, k, I, code):
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_route(16, 16, None, d, 16, 16, stream=0)
     assert moe.STATUS[ei.value.code] == code
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_expert_ffn_form(d)
+    assert moe.STATUS[ei.value.code] == code
 
 
 def test_pointer_and_workspace_checks(moe):

@@ -56,16 +56,19 @@ def test_shared_expert_vs_oracle(moe, Is, G, T):
     assert_close_f32(got, ref)
 
 
-def test_shared_expert_equals_routed_path_on_copies(moe):
+@pytest.mark.parametrize("T", [333, 5])
+def test_shared_expert_equals_routed_path_on_copies(moe, T):
     """Shard g of the shared expert, computed with the token rows read in place,
     equals the grouped expert FFN over G copies of the rows with the same packed
-    weights (E = G experts of intermediate Is / G), bit for bit."""
+    weights (E = G experts of intermediate Is / G), bit for bit.  T = 5 runs the
+    GEMMs in their swapped form on both sides."""
     wl = synth.WORKLOADS["ling3_tiny"]
-    T, Is, G = 333, 1024, 8
+    Is, G = 1024, 8
     x = synth.tokens(wl, T)
     p, _ = packed_shared(moe, wl, Is, G)
     got = run_shared(moe, x, p, T, wl.H, Is, G)
     d_rows = moe.dims(G * T, wl.H, G, 1, Is // G)  # G "experts" of Is / G, G * T rows
+    assert moe.moe_expert_ffn_form(d_rows) == (1 if T == 5 else 0)
     ws = moe.new_workspace(d_rows)
     xp = dev_bf16(np.tile(x, (G, 1)))
     offsets = dev(np.arange(G + 1, dtype=np.int32) * T)

@@ -126,13 +126,13 @@ def test_combine(moe, case):
 
 
 def test_route_kernels_agree_bitwise(moe):
-    """Three router kernels: CTA clusters up to 64 tokens, 1D tiles, and (256
-    experts) 2D tiles once every SM gets a CTA (T >= 32 x SMs, 4864 on 152 SMs).
-    Every logit is the same FMA chain in all of them, so a token's experts and
-    weights must be the same bits whichever kernel ran."""
+    """Three router kernels: CTA clusters (1 to 8 tokens each) up to 1024 tokens,
+    1D tiles, and (256 experts) 2D tiles once every SM gets a CTA (T >= 32 x SMs,
+    4864 on 152 SMs).  Every logit is the same FMA chain in all of them, so a
+    token's experts and weights must be the same bits whichever kernel ran."""
     wl = synth.WORKLOADS["large"]
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    Ts = (5, 64, 65, 32 * sms - 1, 32 * sms + 96)
+    Ts = (5, 64, 65, 1024, 1025, 32 * sms - 1, 32 * sms + 96)
     x = synth.tokens(wl, Ts[-1])
     wr, bias = synth.router(wl)
     got = []
