@@ -126,30 +126,42 @@ __device__ __forceinline__ void route_one_token(const float* lrow, const float* 
       taken |= 1u << q;
     }
   }
+  // Selection keys as unsigned integers in the order (value desc): the value
+  // plus 0.0f (so -0 and +0 become one key and tie, as in a float comparison),
+  // its bits made monotone; NaN sorts below every number and padding experts
+  // below everything.  Each round takes the largest key over the warp with one
+  // reduction and, among the lanes holding it, the lowest expert with another:
+  // the order (value desc, expert asc) of the shuffle argmax it replaced, in two
+  // dependent warp operations per round instead of ten.
+  uint32_t key[NV];
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    if ((taken >> q) & 1u) {
+      key[q] = 0u;
+    } else {
+      const float f = __fadd_rn(v[q], 0.0f);
+      const uint32_t u = __float_as_uint(f);
+      key[q] = (f != f) ? 1u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+    }
+  }
   float sel_l[kMaxK];
   int sel_e[kMaxK];
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
     if (j < k) {
-      float bv = -INFINITY;
-      int be = 0x7FFFFFFF;
+      uint32_t bk = 0u;
+      int bq = 0;
 #pragma unroll
       for (int q = 0; q < NV; ++q) {
-        const int e = lane + 32 * q;
-        if (!((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
-          bv = v[q];
-          be = e;
+        if (!((taken >> q) & 1u) && key[q] > bk) {
+          bk = key[q];
+          bq = q;
         }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-        const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
+      const uint32_t cand = (bk == m && !((taken >> bq) & 1u)) ? (uint32_t)(lane + 32 * bq) : 0xFFFFFFFFu;
+      const int be = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
+      float bv;
       if constexpr (KIND == 1) {
         // the winner's pre-bias score, from the lane that owns expert be
         float mine = 0.0f;
@@ -157,6 +169,10 @@ __device__ __forceinline__ void route_one_token(const float* lrow, const float* 
         for (int q = 0; q < NV; ++q)
           if (q == (be >> 5)) mine = sc[q];
         bv = __shfl_sync(0xFFFFFFFFu, mine, be & 31);
+      } else {
+        // the logit back from its key (for -0 this gives +0, which the softmax
+        // below treats identically)
+        bv = __uint_as_float((m & 0x80000000u) ? (m & 0x7FFFFFFFu) : ~m);
       }
       sel_l[j] = bv;
       sel_e[j] = be;
@@ -494,10 +510,8 @@ __global__ void __launch_bounds__(NTHR, 4) route_tile_kernel(const uint16_t* __r
 // (EC*4 contiguous bytes per hidden row), so kCC SMs share the weight traffic that
 // one CTA carried alone.  Thread (tok, el) runs the FMA chain of token tok and
 // expert r*EC + el over h = 0..H-1 (the same chain as the other router kernels),
-// reading W_r and x from a cp.async ring.  The ring holds each W_r chunk
-// transposed (one padded row of HC hidden values per expert), so a thread reads
-// eight consecutive h with two 16-byte loads of W_r and one of x: at T = 1 the
-// kernel's time is this one dependent chain of H FMAs.  The logits go into the first CTA's
+// reading W_r and x from a cp.async ring (16-byte copies; x read eight hidden
+// values per 16-byte load).  The logits go into the first CTA's
 // shared memory (distributed shared memory), and after a cluster barrier its warps
 // run the shared per-token epilogue.
 constexpr int kCC = 8;       // CTAs per cluster
@@ -505,13 +519,12 @@ constexpr int kCC = 8;       // CTAs per cluster
 template <int EP, int TSV>
 struct ClusterCfg {
   static constexpr int EC = EP / kCC;                  // experts per CTA
-  static constexpr int HC = (EP >= 256) ? 64 : 128;    // hidden rows per stage (divides H)
-  static constexpr int HCP = HC + 4;                   // padded row of the transposed chunk
-  static constexpr int CNST = (EP <= 64) ? 12 : 6;     // ring depth: 24-48 KB of W_r in flight
+  static constexpr int HC = (EP >= 256) ? 128 : 256;   // hidden rows per stage
+  static constexpr int CNST = (EP <= 64) ? 6 : 4;      // ring depth: 40-64 KB of W_r in flight
   static constexpr int NCMP = EC * TSV;                // computing threads
   static constexpr int NTH = NCMP < 128 ? 128 : NCMP;  // all of them copy
   static constexpr int LLD = EP + 1;
-  static constexpr int ring = CNST * (EC * HCP * 4 + TSV * HC * 2);
+  static constexpr int ring = CNST * (HC * EC * 4 + TSV * HC * 2);
   static constexpr int bytes = ring + TSV * LLD * 4;
 };
 
@@ -521,42 +534,41 @@ __global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(ClusterCfg<EP, TSV
                          const float* __restrict__ bias, int T, int H, int E, int k, int wbf16,
                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   using C = ClusterCfg<EP, TSV>;
-  constexpr int EC = C::EC, HC = C::HC, HCP = C::HCP, NTH = C::NTH, LLD = C::LLD,
-                CNST = C::CNST;
+  constexpr int EC = C::EC, HC = C::HC, NTH = C::NTH, LLD = C::LLD, CNST = C::CNST;
   extern __shared__ float4 smem_f4[];
-  float* ws = reinterpret_cast<float*>(smem_f4);                    // [CNST][EC][HCP]
-  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + CNST * EC * HCP); // [CNST][TSV][HC]
+  float* ws = reinterpret_cast<float*>(smem_f4);                    // [CNST][HC][EC]
+  uint16_t* xst = reinterpret_cast<uint16_t*>(ws + CNST * HC * EC); // [CNST][TSV][HC]
   float* ls = reinterpret_cast<float*>(xst + CNST * TSV * HC);      // [TSV][LLD], CTA 0's used
   const int tid = threadIdx.x;
   const int rank = (int)cluster_ctarank();
   const int e0 = rank * EC;                  // this CTA's first expert
   const int t0 = (blockIdx.x / kCC) * TSV;   // the cluster's first token
-  const int nchunks = H / HC;
+  const int nchunks = (H + HC - 1) / HC;  // the last one may hold fewer rows (H % 128 == 0)
   const int ecols = max(0, min(EC, E - e0));  // valid experts of this CTA
 
   if (ecols < EC) {  // experts past E read zeros for the whole kernel
-    for (int i = tid; i < CNST * EC * HCP; i += NTH)
-      if ((i / HCP) % EC >= ecols) ws[i] = 0.0f;
+    for (int i = tid; i < CNST * HC * EC; i += NTH)
+      if ((i % EC) >= ecols) ws[i] = 0.0f;
   }
   auto issue_chunk = [&](int c) {
     if (c < nchunks) {
       const int buf = c % CNST;
       const int h0 = c * HC;
-      float* wdst = ws + buf * EC * HCP;
-      // consecutive threads read consecutive experts of one hidden row (coalesced)
-      // and write them transposed, one padded row per expert
-      if (ecols == EC) {
-        for (int i = tid; i < HC * EC; i += NTH) {
-          const int r = i / EC, c2 = i % EC;
-          cp_async_4(wdst + c2 * HCP + r, wr + (size_t)(h0 + r) * E + e0 + c2);
+      const int rows = min(HC, H - h0);
+      float* wdst = ws + buf * HC * EC;
+      if (ecols == EC && (E % 4) == 0) {
+        constexpr int PPR = EC / 4;  // 16-byte pieces per hidden row
+        for (int i = tid; i < rows * PPR; i += NTH) {
+          const int r = i / PPR, pc = i % PPR;
+          cp_async_16(wdst + r * EC + 4 * pc, wr + (size_t)(h0 + r) * E + e0 + 4 * pc, 16);
         }
       } else {
-        for (int i = tid; i < HC * ecols; i += NTH) {
+        for (int i = tid; i < rows * ecols; i += NTH) {
           const int r = i / ecols, c2 = i % ecols;
-          cp_async_4(wdst + c2 * HCP + r, wr + (size_t)(h0 + r) * E + e0 + c2);
+          cp_async_4(wdst + r * EC + c2, wr + (size_t)(h0 + r) * E + e0 + c2);
         }
       }
-      constexpr int XPR = HC / 8;  // 16-byte pieces per x row
+      const int XPR = rows / 8;  // 16-byte pieces per x row
       uint16_t* xdst = xst + buf * TSV * HC;
       for (int i = tid; i < TSV * XPR; i += NTH) {
         const int r = i / XPR, pc = i % XPR;
@@ -574,25 +586,24 @@ __global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(ClusterCfg<EP, TSV
   for (int c = 0; c < CNST - 1; ++c) issue_chunk(c);
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c % CNST;
+    const int rows = min(HC, H - c * HC);
     issue_chunk(c + CNST - 1);
     cp_async_wait<CNST - 1>();
     __syncthreads();
     if (tid < C::NCMP) {
-      const float* wsb = ws + buf * EC * HCP + el * HCP;
+      const float* wsb = ws + buf * HC * EC + el;
       const uint16_t* xsb = xst + buf * TSV * HC + tok * HC;
 #pragma unroll 4
-      for (int hh = 0; hh < HC; hh += 8) {
+      for (int hh = 0; hh < rows; hh += 8) {
         const uint4 xv = *reinterpret_cast<const uint4*>(xsb + hh);
-        const float4 w0 = *reinterpret_cast<const float4*>(wsb + hh);
-        const float4 w1 = *reinterpret_cast<const float4*>(wsb + hh + 4);
-        acc = fmaf(bf16_lo(xv.x), w0.x, acc);
-        acc = fmaf(bf16_hi(xv.x), w0.y, acc);
-        acc = fmaf(bf16_lo(xv.y), w0.z, acc);
-        acc = fmaf(bf16_hi(xv.y), w0.w, acc);
-        acc = fmaf(bf16_lo(xv.z), w1.x, acc);
-        acc = fmaf(bf16_hi(xv.z), w1.y, acc);
-        acc = fmaf(bf16_lo(xv.w), w1.z, acc);
-        acc = fmaf(bf16_hi(xv.w), w1.w, acc);
+        acc = fmaf(bf16_lo(xv.x), wsb[(hh + 0) * EC], acc);
+        acc = fmaf(bf16_hi(xv.x), wsb[(hh + 1) * EC], acc);
+        acc = fmaf(bf16_lo(xv.y), wsb[(hh + 2) * EC], acc);
+        acc = fmaf(bf16_hi(xv.y), wsb[(hh + 3) * EC], acc);
+        acc = fmaf(bf16_lo(xv.z), wsb[(hh + 4) * EC], acc);
+        acc = fmaf(bf16_hi(xv.z), wsb[(hh + 5) * EC], acc);
+        acc = fmaf(bf16_lo(xv.w), wsb[(hh + 6) * EC], acc);
+        acc = fmaf(bf16_hi(xv.w), wsb[(hh + 7) * EC], acc);
       }
     }
     __syncthreads();
