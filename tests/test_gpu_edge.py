@@ -78,6 +78,16 @@ def test_max_experts_and_k(moe):
     layer_vs_oracle(moe, wl)
 
 
+@pytest.mark.parametrize("name,T,E,k", [("one_expert", 5, 1, 1), ("k_is_E", 2, 8, 8),
+                                        ("max_E_k", 8, 256, 16)])
+def test_degenerate_shapes_in_swapped_form(moe, name, T, E, k):
+    """The same degenerate expert counts at H = 256, where small batches run the
+    GEMMs with the weight rows on the MMA's M side."""
+    wl = synth.Workload(name, T=T, H=256, E=E, k=k, I=128, w_std=0.05, wr_std=0.5)
+    assert moe.moe_expert_ffn_form(moe.dims(T, wl.H, E, k, wl.I)) == 1
+    layer_vs_oracle(moe, wl)
+
+
 def test_caller_supplied_routing(moe):
     """Router replay: permute, expert FFN and combine driven by indices and
     weights that did not come from moe_route (here: uniform random distinct
