@@ -46,18 +46,26 @@ namespace {
 
 constexpr int SK = 64;                       // k-block: one 128-byte swizzle row
 constexpr int SUK = 16;                      // MMA K
-constexpr int WROWS = 256;                   // weight rows per unit (one packed box)
+constexpr int WROWS = 256;                   // rows of one packed weight box
 constexpr int HALF = 128;                    // MMA M
 constexpr int TT = 64;                       // token rows per unit at most (MMA N <= 64)
-constexpr int STAGES = 5;
-constexpr int W_BYTES = WROWS * SK * 2;      // 32 KB
 constexpr int X_BYTES = TT * SK * 2;         // 8 KB (N = 64)
-constexpr int ACC_COLS = 2 * TT;             // one accumulator buffer: two halves of N <= 64
-constexpr int TMEM_COLS = 2 * ACC_COLS;      // double-buffered
-constexpr int NBAR = 2 * STAGES + 2 + 2 + 1;
-constexpr int SMEM_BYTES =
-    1024 + STAGES * (W_BYTES + X_BYTES) + NBAR * 8 + 16 + 3 * (kMaxE + 1) * 4;
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+
+// HV halves of a packed box per unit: 2 (a whole box; gate and up must meet in one
+// CTA) or 1 (one 128-row half: twice the units, for the down GEMM when whole-box
+// units would leave most SMs idle).
+template <int HV>
+struct SwapCfg {
+  static constexpr int UROWS = HALF * HV;              // weight rows per unit
+  static constexpr int STAGES = HV == 2 ? 5 : 8;
+  static constexpr int W_BYTES = UROWS * SK * 2;       // 32 or 16 KB
+  static constexpr int ACC_COLS = HV * TT;             // one accumulator buffer
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;       // double-buffered
+  static constexpr int NBAR = 2 * STAGES + 2 + 2 + 1;
+  static constexpr int SMEM_BYTES =
+      1024 + STAGES * (W_BYTES + X_BYTES) + NBAR * 8 + 16 + 3 * (kMaxE + 1) * 4;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
 
 // Weight boxes (256 rows) and token boxes of 16, 32 and 64 rows; all 64 columns.
 struct SwapMaps {
@@ -72,6 +80,7 @@ struct SwapWork {
   int w_load_row;  // box row of k-block 0 in the packed weights
 };
 
+template <int HV>
 __device__ __forceinline__ SwapWork swap_decode(int u, const int* s_prefix, const int* s_off,
                                                 const int* s_tt, int E, int NTW, int KB,
                                                 int a_local) {
@@ -92,7 +101,9 @@ __device__ __forceinline__ SwapWork swap_decode(int u, const int* s_prefix, cons
   w.rows = min(TT, s_off[lo + 1] - w.row0);
   w.nb = w.rows <= 16 ? 16 : (w.rows <= 32 ? 32 : 64);
   w.x_load_row = w.row0 - (a_local ? s_off[lo] : 0);
-  w.w_load_row = (lo * NTW + w.wt) * KB * WROWS;
+  // box row of (expert, box column, k-block 0), plus the half within the box
+  const int NTB = NTW * HV / 2;  // packed boxes per expert
+  w.w_load_row = (lo * NTB + (w.wt * HV >> 1)) * KB * WROWS + (HV == 1 ? (w.wt & 1) * HALF : 0);
   return w;
 }
 
@@ -108,12 +119,15 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, int HV>
 __global__ void __launch_bounds__(192, 1)
     grouped_gemm_swap_kernel(const __grid_constant__ SwapMaps maps,
                              const int32_t* __restrict__ offsets, int E, int R, int n_per_expert,
                              int K, void* __restrict__ out, int out_ld, int32_t* status,
                              long long spin_limit, int a_local) {
+  using C = SwapCfg<HV>;
+  static_assert(!SWIGLU || HV == 2, "gate and up rows of a unit must meet in one CTA");
+  constexpr int STAGES = C::STAGES, W_BYTES = C::W_BYTES, ACC_COLS = C::ACC_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -125,14 +139,14 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_off = s_prefix + (kMaxE + 1);
   int* s_tt = s_off + (kMaxE + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NTW = n_per_expert / WROWS;
+  const int NTW = n_per_expert / C::UROWS;  // units per expert (and token tile)
   const int KB = K / SK;
 
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = __ldg(offsets + e);
@@ -173,7 +187,7 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tensormap(&maps.x32);
     prefetch_tensormap(&maps.x64);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(192, 1)
       int it = 0;
       bool aborted = false;
       for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
-        const SwapWork w = swap_decode(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
+        const SwapWork w = swap_decode<HV>(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
         const CUtensorMap* xm = w.nb == 16 ? &maps.x16 : (w.nb == 32 ? &maps.x32 : &maps.x64);
         const uint32_t bytes = W_BYTES + w.nb * SK * 2;
         for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -211,7 +225,7 @@ __global__ void __launch_bounds__(192, 1)
       // ---------------------------------------------------------- MMA issuer
       int it = 0, tcount = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
-        const SwapWork w = swap_decode(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
+        const SwapWork w = swap_decode<HV>(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
         const uint32_t idesc = idesc_bf16_f32(HALF, w.nb);
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
@@ -234,8 +248,9 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t xd = sdesc_k_major_sw128(x_addr + kk * SUK * 2);
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             mma_bf16(d0, sdesc_k_major_sw128(w_addr + kk * SUK * 2), xd, idesc, accum);
-            mma_bf16(d0 + TT, sdesc_k_major_sw128(w_addr + HALF * 128 + kk * SUK * 2), xd, idesc,
-                     accum);
+            if constexpr (HV == 2)
+              mma_bf16(d0 + TT, sdesc_k_major_sw128(w_addr + HALF * 128 + kk * SUK * 2), xd,
+                       idesc, accum);
           }
           mma_commit(&empty[s]);
         }
@@ -251,7 +266,7 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;
     int tcount = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
-      const SwapWork w = swap_decode(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
+      const SwapWork w = swap_decode<HV>(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       int ok = 1;
@@ -280,9 +295,9 @@ __global__ void __launch_bounds__(192, 1)
         }
       } else {
         // half c: output columns wt * 256 + 128 c + 32 q + lane
-        float* y = static_cast<float*>(out) + (size_t)w.wt * WROWS + q * 32 + lane;
+        float* y = static_cast<float*>(out) + (size_t)w.wt * C::UROWS + q * 32 + lane;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < HV; ++c) {
           for (int j0 = 0; j0 < w.nb; j0 += 16) {
             uint32_t v[16];
             tmem_ld_32x32b_x16(taddr + c * TT + j0, v);
@@ -304,16 +319,17 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, int HV>
 cudaError_t launch_swap(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets, int E,
                         int R, int n_per_expert, int K, void* out, int out_ld, int32_t* status,
                         long long spin_limit, cudaStream_t s, int a_local) {
   SwapMaps m;
-  if (!b.encode(&m.w, WROWS) || !a.encode(&m.x16, 16) || !a.encode(&m.x32, 32) ||
+  using C = SwapCfg<HV>;
+  if (!b.encode(&m.w, C::UROWS) || !a.encode(&m.x16, 16) || !a.encode(&m.x32, 32) ||
       !a.encode(&m.x64, TT))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
@@ -321,17 +337,17 @@ cudaError_t launch_swap(const GemmOperand& a, const GemmOperand& b, const int32_
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !attr_set[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_swap_kernel<SWIGLU>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    err = cudaFuncSetAttribute(grouped_gemm_swap_kernel<SWIGLU, HV>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_set[dev] = true;
   }
   // units <= weight columns x (experts with rows + R / TT): one CTA per unit up to
   // one per SM (the kernel is persistent beyond that)
   const long long units =
-      (long long)(n_per_expert / WROWS) * (std::min<long long>(E, R) + R / TT);
+      (long long)(n_per_expert / C::UROWS) * (std::min<long long>(E, R) + R / TT);
   const int grid = (int)std::max<long long>(1, std::min<long long>(device_sm_count(), units));
-  grouped_gemm_swap_kernel<SWIGLU><<<grid, 192, SMEM_BYTES, s>>>(
+  grouped_gemm_swap_kernel<SWIGLU, HV><<<grid, 192, C::SMEM_BYTES, s>>>(
       m, offsets, E, R, n_per_expert, K, out, out_ld, status, spin_limit, a_local);
   return cudaGetLastError();
 }
@@ -355,7 +371,7 @@ cudaError_t launch_gemm_gate_up_swap(const GemmOperand& a, const GemmOperand& b,
                                      int32_t* status, long long spin_limit, cudaStream_t s,
                                      bool a_local) {
   if (R == 0) return cudaSuccess;
-  return launch_swap<true>(a, b, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
+  return launch_swap<true, 2>(a, b, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
                            a_local ? 1 : 0);
 }
 
@@ -363,7 +379,11 @@ cudaError_t launch_gemm_down_swap(const GemmOperand& a, const GemmOperand& b,
                                   const int32_t* offsets, int E, int R, int H, int I, float* y,
                                   int32_t* status, long long spin_limit, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
-  return launch_swap<false>(a, b, offsets, E, R, H, I, y, H, status, spin_limit, s, 0);
+  // half-box units while whole-box units would fill at most half of the SMs
+  // (experts with rows <= min(E, R)); each row's chain and epilogue are the same
+  if (2LL * (H / WROWS) * std::min(E, R) <= device_sm_count())
+    return launch_swap<false, 1>(a, b, offsets, E, R, H, I, y, H, status, spin_limit, s, 0);
+  return launch_swap<false, 2>(a, b, offsets, E, R, H, I, y, H, status, spin_limit, s, 0);
 }
 
 }  // namespace moe
