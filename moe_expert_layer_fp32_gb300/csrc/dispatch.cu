@@ -181,35 +181,54 @@ __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __res
   uint32_t* masks = smem_u;
   int32_t* sidx = reinterpret_cast<int32_t*>(smem_u + 8 * E);
   __shared__ int s_scan[kMaxE];
+  __shared__ int s_wsum[PB / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = blockIdx.x * 8 + warp;  // this warp's token (copy phase)
+  // The token's source row does not depend on the routing: its first 32 x U
+  // 16-byte vectors are loaded now, and land while the CTA ranks.
+  constexpr int U = 8;
+  const int nv = H / 8;  // 16-byte vectors per row
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t < T ? t : 0) * H);
+  uint4 v0[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int cc = u * 32 + lane;
+    if (t < T && cc < nv) v0[u] = __ldg(src + cc);
+  }
   // every CTA ranks the whole (single) block; each then copies its own 8 tokens
   build_masks(topk_idx, T, k, E, 0, masks, sidx, blockIdx.x == 0 ? status : nullptr);
-  const int tid = threadIdx.x;
   int c = 0;
   if (tid < E) {
 #pragma unroll
     for (int w = 0; w < 8; ++w) c += __popc(masks[w * E + tid]);
   }
-  s_scan[tid] = c;  // blockDim == kMaxE
-  __syncthreads();
-  for (int off = 1; off < kMaxE; off <<= 1) {
-    const int v = (tid >= off) ? s_scan[tid - off] : 0;
-    __syncthreads();
-    s_scan[tid] += v;
-    __syncthreads();
+  // exclusive scan over the experts (blockDim == kMaxE): within each warp by
+  // shuffles, then over the eight warp totals
+  int incl = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += n;
   }
-  const int excl = s_scan[tid] - c;
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int total = 0;
+#pragma unroll
+  for (int w = 0; w < PB / 32; ++w) {
+    const int sw = s_wsum[w];
+    if (w < warp) incl += sw;
+    total += sw;
+  }
+  const int excl = incl - c;
   if (blockIdx.x == 0) {
     if (tid < E) {
       counts[tid] = c;
       offsets[tid] = excl;
     }
-    if (tid == 0) offsets[E] = s_scan[kMaxE - 1];
+    if (tid == 0) offsets[E] = total;
   }
-  __syncthreads();
   s_scan[tid] = excl;  // first row of each expert
   __syncthreads();
-  const int lane = tid & 31;
-  const int t = blockIdx.x * 8 + (tid >> 5);  // this warp's token
   if (t >= T) return;
   const long long R = (long long)T * k;
   // lane j < k ranks slot (t, j): the token sits in mask word t / 32, bit t % 32
@@ -228,15 +247,13 @@ __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __res
     row_of_slot[sl] = my_row;
     if (my_row >= 0) slot_of_row[my_row] = (int32_t)sl;
   }
-  const int nv = H / 8;  // 16-byte vectors per row
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  constexpr int U = 8;
   for (int c0 = 0; c0 < nv; c0 += 32 * U) {
     uint4 v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int cc = c0 + u * 32 + lane;
-      if (cc < nv) v[u] = __ldg(src + cc);
+      if (c0 == 0) v[u] = v0[u];
+      else if (cc < nv) v[u] = __ldg(src + cc);
     }
     for (int j = 0; j < k; ++j) {
       const int r = __shfl_sync(0xFFFFFFFFu, my_row, j);
