@@ -23,6 +23,9 @@
 // one MMA per half into two TMEM accumulators of N columns (double-buffered).
 // Units are numbered expert-major, then weight column, then token tile, so the
 // token tiles of one weight column run side by side and share its L2 lines.
+// For the down GEMM, when whole-box units would fill at most half of the SMs, a
+// unit is one 128-row half of a box (HV = 1): one MMA per K step, twice the
+// units, the same chain and epilogue per element.
 //
 // Each output element is the same K order (64-wide k-blocks ascending, 16-wide
 // MMAs ascending, FP32 accumulation from zero) over the same BF16 products as in

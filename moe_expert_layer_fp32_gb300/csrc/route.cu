@@ -11,13 +11,14 @@
 // of the bias, and both finish with the same per-token epilogue: the routing of
 // a token is the same bits whichever kernel runs and whatever T is.
 //
-// route_kernel (T large): one CTA = 32 tokens x all E experts (E padded to EP
+// route_kernel (T > 1024): one CTA = 32 tokens x all E experts (E padded to EP
 // in {32, 64, 128, 256}); 128 threads = 4 warps, up to four CTAs per SM.  Warp w
 // owns tokens 8w..8w+7; lane i owns EP/32 experts (4i + 128g + jj for EP >= 128,
-// else EP/32 consecutive).  Chunks of HK = 4096/EP hidden columns (16 KB of W_r)
-// and the matching x columns are copied by cp.async into a 3-stage ring while
-// earlier chunks are multiplied (four CTAs fit on an SM); x is widened once to FP32 into a transposed
-// buffer, so a warp's eight token values for one h are two broadcast loads.
+// else EP/32 consecutive).  Chunks of HK = max(2048/EP, 16) hidden columns (8-16
+// KB of W_r) and the matching x columns are copied by cp.async into a 3-stage
+// ring while earlier chunks are multiplied (four CTAs fit on an SM); x is widened
+// once to FP32 into a transposed buffer, so a warp's eight token values for one h
+// are two broadcast loads.
 //
 // route_cluster_kernel (T <= 1024): a cluster of eight CTAs per 1, 2, 4 or 8
 // tokens, each CTA owning an eighth of the experts and streaming only those
@@ -26,7 +27,8 @@
 // route_tile_kernel (256 experts, large T): 2D warp tiles (see below).
 //
 // Epilogue (shared): logits go to shared memory; one warp per token runs k
-// rounds of a warp-wide argmax under the key (logit desc, expert asc), then the
+// rounds of a warp-wide selection under the key (logit desc, expert asc), each
+// a redux.sync max over a monotone integer key and a min over the expert, then the
 // softmax denominator (lane partial sums in ascending expert order, then an xor
 // butterfly: identical bits on every lane and for every T).  Selection uses the
 // FP32 logit, which orders experts exactly as the probabilities do.
