@@ -595,8 +595,8 @@ __global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(ClusterCfg<EP, TSV
     if (tid < C::NCMP) {
       const float* wsb = ws + buf * HC * EC + el;
       const uint16_t* xsb = xst + buf * TSV * HC + tok * HC;
-#pragma unroll 4
-      for (int hh = 0; hh < rows; hh += 8) {
+      // eight hidden rows of the chain: the same FMAs in the same order either way
+      auto step8 = [&](int hh) {
         const uint4 xv = *reinterpret_cast<const uint4*>(xsb + hh);
         acc = fmaf(bf16_lo(xv.x), wsb[(hh + 0) * EC], acc);
         acc = fmaf(bf16_hi(xv.x), wsb[(hh + 1) * EC], acc);
@@ -606,6 +606,15 @@ __global__ void __cluster_dims__(kCC, 1, 1) __launch_bounds__(ClusterCfg<EP, TSV
         acc = fmaf(bf16_hi(xv.z), wsb[(hh + 5) * EC], acc);
         acc = fmaf(bf16_lo(xv.w), wsb[(hh + 6) * EC], acc);
         acc = fmaf(bf16_hi(xv.w), wsb[(hh + 7) * EC], acc);
+      };
+      if (rows == HC) {
+        // a whole chunk unrolled: every load is visible to the scheduler (an
+        // isolated probe ran this loop at 6.2 instead of 6.9 cycles per FMA)
+#pragma unroll
+        for (int hh = 0; hh < HC; hh += 8) step8(hh);
+      } else {
+#pragma unroll 4
+        for (int hh = 0; hh < rows; hh += 8) step8(hh);
       }
     }
     __syncthreads();
