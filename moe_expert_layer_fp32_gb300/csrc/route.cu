@@ -650,7 +650,10 @@ cudaError_t launch_cluster(const void* x, const float* wr, const float* bias, in
   int dv = 0;
   cudaGetDevice(&dv);
   const int known = dv < 64 ? ok[dv] : 0;
-  if (known < 0) return launch_cluster<EP, TSV, KIND, kCC>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+  if constexpr (CC > kCC) {  // only a non-portable size can be refused
+    if (known < 0)
+      return launch_cluster<EP, TSV, KIND, kCC>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
