@@ -16,6 +16,17 @@ For N > 1 (torchrun), every rank runs its own replica on its own GPU (tokens are
 independent: weak scaling, no collective on the data path); the timed region is
 bracketed by barriers and the max over ranks is taken.
 
+The line's `decode` object times the batch-invariance / decode shapes: the
+fine_grained layer (H=2048, E=64, k=8, I=1024, Zipf(s=1) router bias) at
+T = 1, 8, 64, 512 and 4096, each batch a prefix of the same 4096 seed-0 tokens.
+Each step is one CUDA-graph replay of moe_layer_fwd, preceded (outside its
+events) by a read of a buffer four times the size of L2, which evicts the
+weights and the previous step's dirty lines and leaves only clean lines behind,
+so every step streams its active experts' weights from HBM.  The step is set
+against the HBM weight-streaming roofline: the active experts' weight bytes plus
+the router weights and the tokens in and out, over the measured copy bandwidth.
+Each T's output rows are also compared bytewise with the T = 4096 rows.
+
 --impl reference times the CPU oracle (the plain C++ definition of the layer) on
 the host cores on a bounded sample of tokens of the same workload.
 """
@@ -40,10 +51,12 @@ import synth  # noqa: E402
 
 METRIC = "routed tokens/s per MoE layer fwd"
 
-# DRAM bytes per launch of the gate/up GEMM on the large workload, from one ncu
-# capture (profiles/gemm_dram_traffic_large.md), valid while the kernel sources
-# are unchanged since the capture.
-GEMM_TRAFFIC_LARGE = {"bytes": 11566245888 + 1070497536, "sources_sha256_16": "1a80c7875a5ad7e8"}
+# DRAM bytes (read + write) per launch of the gate/up GEMM on the large workload:
+# one ncu capture of the same kernel on large-shaped rows at one eighth of the
+# size (E = 32 experts, T = 4096 tokens: the same 1024 rows per expert, H and I),
+# scaled by 8, the ratio of both the rows and the expert weights.  Valid while
+# the kernel sources are unchanged since the capture; None until it is taken.
+GEMM_TRAFFIC_LARGE = None
 
 
 def gemm_sources_hash():
@@ -65,6 +78,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-decode", action="store_true",
+                   help="leave out the decode-shape sweep (fine_grained layer, T = 1 .. 4096)")
     p.add_argument("--tokens", type=int, default=None,
                    help="override T of the workload (smaller cases for profiling)")
     p.add_argument("--flush-l2", action="store_true",
@@ -289,6 +304,85 @@ def run_reference(args):
     return 0
 
 
+# ---------------------------------------------------------- decode shapes ---
+DECODE_TS = (1, 8, 64, 512, 4096)
+
+
+def decode_sweep(moe, torch, hbm_gbs, steps):
+    """The fine_grained layer at T = 1 .. 4096 (prefixes of one token batch): per
+    T, the mean device time of `steps` CUDA-graph replays of moe_layer_fwd, each
+    after a clean L2 flush, against the HBM weight-streaming roofline."""
+    wl = synth.WORKLOADS["fine_grained"]
+    H, E, k, I = wl.H, wl.E, wl.k, wl.I
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(
+        torch.bfloat16)
+    wg, wu, wd = synth.expert_weights(wl)
+    d_max = moe.dims(max(DECODE_TS), H, E, k, I)
+    wg_d, wu_d, wd_d = to_dev(wg), to_dev(wu), to_dev(wd)
+    del wg, wu, wd
+    packed = moe.prepack(wg_d, wu_d, wd_d, d_max)
+    del wg_d, wu_d, wd_d
+    wr, bias = synth.router(wl)
+    wr_d, bias_d = torch.from_numpy(wr).cuda(), torch.from_numpy(bias).cuda()
+    x_all = to_dev(synth.tokens(wl, max(DECODE_TS)))
+    # read-only flush: four times L2, summed (only clean lines are left in L2)
+    flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
+    runs = {}
+    for T in sorted(DECODE_TS, reverse=True):
+        d = moe.dims(T, H, E, k, I)
+        ws = moe.new_workspace(d)
+        x = x_all[:T].clone()
+        out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        counts = torch.empty(E, dtype=torch.int32, device="cuda")
+
+        def step():
+            moe.moe_layer_fwd(x, wr_d, bias_d, packed, d, out, None, None, counts, ws)
+
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            flush.sum()
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            flush.sum()
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        if moe.moe_read_device_status(ws) != 0:
+            raise RuntimeError(f"device status after the decode steps at T={T}")
+        us = 1e3 * statistics.mean(a.elapsed_time(b) for a, b in ev)
+        active = int((counts > 0).sum().item())
+        stream_bytes = active * 3 * H * I * 2 + H * E * 4 + 2 * T * H * 2
+        runs[T] = {"T": T, "step_us": us, "routed_tokens_per_s": T * k / (us / 1e6),
+                   "active_experts": active, "weight_stream_bytes": stream_bytes,
+                   "achieved_gbs": stream_bytes / (us / 1e6) / 1e9,
+                   "frac": stream_bytes / (us / 1e6) / 1e9 / hbm_gbs,
+                   "out": out.view(torch.int16).cpu().numpy()}
+        del g, ws
+    ref = runs[max(DECODE_TS)]["out"]
+    for T, r in runs.items():
+        r["rows_equal_T4096"] = bool(np.array_equal(r.pop("out"), ref[:T]))
+    return {"workload": f"fine_grained layer: H={H} E={E} k={k} I={I}, Zipf(s=1) router bias; "
+                        "tokens = prefixes of one 4096-token batch",
+            "timing": f"mean of {steps} CUDA-graph replays of moe_layer_fwd per T, each after "
+                      "a 512 MB read (clean L2 flush) outside its events",
+            "roofline": "HBM weight streaming: active experts' weights + router weights + "
+                        "tokens in and out, over the measured copy bandwidth",
+            "peak_gbs": hbm_gbs,
+            "rows_bitwise_batch_invariant": all(r["rows_equal_T4096"] for r in runs.values()),
+            "points": [runs[T] for T in DECODE_TS]}
+
+
 # -------------------------------------------------------------- our arm ---
 def run_ours(args):
     import torch
@@ -453,10 +547,12 @@ def run_ours(args):
                 "achieved": achieved, "peak": bf16_burst, "unit": "TFLOP/s",
                 "frac": achieved / bf16_burst,
                 "traffic": (GEMM_TRAFFIC_LARGE["bytes"]
-                            if wl.name == "large" and gemm_sources_hash()
-                            == GEMM_TRAFFIC_LARGE["sources_sha256_16"] else None),
-                "traffic_note": "DRAM read+write bytes per launch, ncu capture "
-                                "(profiles/gemm_dram_traffic_large.md); algorithmic "
+                            if GEMM_TRAFFIC_LARGE is not None and wl.name == "large"
+                            and gemm_sources_hash() == GEMM_TRAFFIC_LARGE["sources_sha256_16"]
+                            else None),
+                "traffic_note": "DRAM read+write bytes per launch: ncu capture at 1/8 size "
+                                "(E=32, T=4096, same rows per expert), scaled by 8; "
+                                "algorithmic "
                                 f"{(4.0 * E * H * I + R * H * 2 + R * I * 2) / 1e9:.2f} GB",
                 "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)" if src == "measured"
                 else "fallback bf16 burst",
@@ -519,6 +615,10 @@ def run_ours(args):
                    " per step; pinned host tokens copied in and outputs copied out, transfers "
                    "overlapped with compute)"}
 
+    decode = None
+    if world == 1 and not args.no_decode and args.shards <= 0:
+        decode = decode_sweep(moe, torch, hbm, max(10, K))
+
     cpu = None
     if want_cpu:
         host_w = host_weight_fn(wl, full_host)
@@ -545,7 +645,7 @@ def run_ours(args):
                 "config": workload_config(wl, world, l2, shard),
                 "tokens_per_s": world * T * K / (total_ms / 1e3),
                 "roofline": roofline, "grouped_gemm_tflops": grouped, "stages": stages,
-                "weight_stream": weight_stream, "graph": graph_note,
+                "weight_stream": weight_stream, "graph": graph_note, "decode": decode,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * K,
                 "clocks": clock_info}
         print(json.dumps(line))

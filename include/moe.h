@@ -373,9 +373,13 @@ moe_status moe_layer_fwd_profiled(const void* x, const float* w_router, const fl
  *   device_status: optional device int32 (NULL: not reported); receives
  *   MOE_ERR_DEVICE_CHECK if an expert id is out of range or repeated within a
  *   token (the caller zeroes it beforehand).
+ * Arguments are checked as moe_load_stats checks them (dims, non-null 16-byte
+ * aligned pointers, an sm_103 device), and device_status too when given.
  * The first call on each device looks up the scratch array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.  All
- * calls on a device share the one scratch array, and each call overwrites the
+ * (cudaGetSymbolAddress) and keeps it for the process; make that first call
+ * before any stream capture, and do not call this entry point again on a device
+ * after cudaDeviceReset on it (the kept address belonged to the old context).
+ * All calls on a device share the one scratch array, and each call overwrites the
  * part of it that it reads, so calls whose kernels can overlap on the GPU (other
  * streams, other host threads) race: serialise them.  Nothing is allocated or
  * freed. */

@@ -27,23 +27,10 @@
 // zeros there); those rows are computed but never stored, and a row's result
 // does not depend on the other rows of its tile.
 //
-// CL = 2 (used when N/BN is even): CTAs work in clusters of two that split the
-// L2->SM traffic of a pair of tiles sharing an operand.  Work units, numbered
-// expert-major:
-//   "B-shared": row tiles 2p and 2p+1 of expert e with the same column tile; each
-//               CTA loads its own A tile and one half of the B tile, multicast
-//               to both CTAs;
-//   "A-shared": an expert's odd last row tile with column tiles 2j and 2j+1;
-//               each CTA loads its own B tile and one half of the A tile,
-//               multicast to both.
-// Either way each CTA's stage still holds a full A and B tile and runs the same
-// cta_group::1 MMAs, so the arithmetic is unchanged; a stage is refilled only
-// after both CTAs' MMAs have released it (multicast commit, 2 arrivals).
-// CL = 1: every CTA loads its own tiles (odd N/BN).
-//
 // A pair variant (grouped_gemm_pair_kernel, below) runs one M=256 MMA across the
-// two CTAs of a cluster (cta_group::2); launch_gemm_down uses it where it measured
-// faster.
+// two CTAs of a cluster (cta_group::2); the launchers use it where it measured
+// faster.  Every TMA load of both kernels writes only the issuing CTA's own shared
+// memory (no cluster multicast).
 //
 // The tile shape, K order (k-blocks ascending, 16-wide MMAs ascending) and N
 // split depend only on H and I, never on T: batch-invariant by construction.
@@ -52,7 +39,7 @@
 // CTA-wide abort flag and records MOE_ERR_TIMEOUT; the roles then drain their own
 // in-flight TMA copies and MMAs (bounded by the fixed default limit, whatever
 // spin_limit is) before TMEM is released, and
-// the two CTAs of a cluster meet at a cluster barrier before either exits.
+// the two CTAs of a pair meet at a cluster barrier before either exits.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -75,31 +62,33 @@ struct Cfg {
   static constexpr int EPI_LD = 36;
   static constexpr int EPI_BYTES = 4 * 32 * EPI_LD * 4;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NBAR * 8 + 16 +
-                                    3 * (kMaxE + 1) * 4;
+                                    2 * (kMaxE + 1) * 4;
 };
 
-// Tensor maps of one grouped GEMM: A (rows of x_perm or h) in boxes of 128 and
-// 64 rows, B (packed weight rows) in boxes of BN and BN/2 rows; all 64 columns.
+// Tensor maps of one grouped GEMM: A (rows of x_perm or h) in boxes of 128 rows,
+// B (packed weight rows) in boxes of BN rows (single-CTA kernel) or BN/2 rows (one
+// CTA's half of the pair kernel's tile); all 64 columns.
 struct Maps {
-  CUtensorMap a128, a64, b_full, b_half;
+  CUtensorMap a128, b_tile;
 };
 
-// One CTA's share of a work unit.
+// One work unit of the single-CTA kernel: one 128-row tile of one expert's rows
+// times one BN-column tile.
 struct Work {
-  int e, nt;       // expert, this CTA's column tile
-  int a_row0;      // first row of this CTA's row tile
+  int e, nt;       // expert, column tile
+  int a_row0;      // first output row of the tile
   int rows;        // rows of the tile that belong to expert e
-  int mode;        // 0: own tiles, 1: B-shared, 2: A-shared
-  int a_load_row;  // first row of the A box this CTA issues
-  int b_load_row;  // first row of the B box this CTA issues
+  int a_load_row;  // first row of the A box
+  int b_load_row;  // box row of k-block 0 in the packed weights
 };
 
+// Units are numbered expert-major, then row tile, then column tile.
 // a_local: every group reads A rows from 0 (one A operand shared by all groups,
 // e.g. the token rows of a shared expert split into column shards); otherwise a
 // group's A rows are its output rows.
-template <int BN, int CL>
-__device__ __forceinline__ Work decode(int u, int rank, const int* s_prefix, const int* s_off,
-                                       const int* s_mt, int E, int NT, int KB, int a_local) {
+template <int BN>
+__device__ __forceinline__ Work decode(int u, const int* s_prefix, const int* s_off, int E, int NT,
+                                       int KB, int a_local) {
   // largest e with s_prefix[e] <= u (experts without work share the next prefix)
   int lo = 0, hi = E - 1;
   while (lo < hi) {
@@ -108,35 +97,16 @@ __device__ __forceinline__ Work decode(int u, int rank, const int* s_prefix, con
     else hi = mid - 1;
   }
   const int local = u - s_prefix[lo];
+  const int mt = local / NT;
   Work w;
   w.e = lo;
-  int mt;
-  if constexpr (CL == 1) {
-    mt = local / NT;
-    w.nt = local - mt * NT;
-    w.mode = 0;
-  } else {
-    const int nB = (s_mt[lo] >> 1) * NT;
-    if (local < nB) {
-      // column-tile-major: consecutive clusters share one B tile (2 MB of weights)
-      // while it is in L2; the expert's rows (A) stay in L2 across its column tiles
-      const int MP = s_mt[lo] >> 1;
-      w.nt = local / MP;
-      const int mp = local - w.nt * MP;
-      mt = 2 * mp + rank;
-      w.mode = 1;
-    } else {
-      mt = s_mt[lo] - 1;
-      w.nt = 2 * (local - nB) + rank;
-      w.mode = 2;
-    }
-  }
+  w.nt = local - mt * NT;
   w.a_row0 = s_off[lo] + mt * GM;
   w.rows = min(GM, s_off[lo + 1] - w.a_row0);
-  w.a_load_row = w.a_row0 - (a_local ? s_off[lo] : 0) + (w.mode == 2 ? rank * (GM / 2) : 0);
+  w.a_load_row = w.a_row0 - (a_local ? s_off[lo] : 0);
   // B is packed box by box: (expert, column tile, k-block) -> BN contiguous rows of
   // 64 K values; this is the box row of k-block 0 (k-block kb adds kb * BN)
-  w.b_load_row = (lo * NT + w.nt) * KB * BN + (w.mode == 1 ? rank * (BN / 2) : 0);
+  w.b_load_row = (lo * NT + w.nt) * KB * BN;
   return w;
 }
 
@@ -204,7 +174,7 @@ __device__ __forceinline__ void epilogue_block(uint32_t taddr, int row0, int nt,
   }
 }
 
-template <int BN, bool SWIGLU, int CL>
+template <int BN, bool SWIGLU>
 __global__ void __launch_bounds__(192, 1)
     grouped_gemm_kernel(const __grid_constant__ Maps maps, const int32_t* __restrict__ offsets,
                         int E, int R, int n_per_expert, int K, void* __restrict__ out, int out_ld,
@@ -226,13 +196,10 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_off = s_prefix + (kMaxE + 1);
-  int* s_mt = s_off + (kMaxE + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = n_per_expert / BN;
   const int KB = K / GK;
-  const int rank = (CL == 2) ? (int)cluster_ctarank() : 0;
-  const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
 
   // all threads bring the offsets in at once; thread 0 then builds the schedule from
   // shared memory (a serial walk over global memory would cost E load latencies)
@@ -245,10 +212,8 @@ __global__ void __launch_bounds__(192, 1)
     for (int e = 0; e < E; ++e) {
       const int a = s_off[e], b = s_off[e + 1];
       if (b < a) ok = false;
-      const int mt = b > a ? (b - a + GM - 1) / GM : 0;
-      s_mt[e] = mt;
       s_prefix[e] = p;
-      p += mt * NT / CL;  // CL == 2 only when NT is even
+      p += (b > a ? (b - a + GM - 1) / GM : 0) * NT;
     }
     if (!ok) {
       flag_error(status, MOE_ERR_DEVICE_CHECK);
@@ -259,7 +224,7 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CL);
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -270,16 +235,11 @@ __global__ void __launch_bounds__(192, 1)
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&maps.a128);
-    prefetch_tensormap(&maps.b_full);
-    if constexpr (CL == 2) {
-      prefetch_tensormap(&maps.a64);
-      prefetch_tensormap(&maps.b_half);
-    }
+    prefetch_tensormap(&maps.b_tile);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  if constexpr (CL == 2) cluster_sync();  // the peer's barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = s_prefix[E];
@@ -289,8 +249,8 @@ __global__ void __launch_bounds__(192, 1)
       // ------------------------------------------------------------ producer
       int it = 0;  // k-blocks issued
       bool aborted = false;
-      for (int u = unit0; u < total && !aborted; u += unit_step) {
-        const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, KB, a_local);
+      for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
+        const Work w = decode<BN>(u, s_prefix, s_off, E, NT, KB, a_local);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -299,20 +259,8 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-          uint8_t* a_dst = sA + s * C::A_BYTES;
-          uint8_t* b_dst = sB + s * C::B_BYTES;
-          if (w.mode == 2) {
-            tma_load_2d_multicast(&maps.a64, a_dst + rank * (GM / 2) * 128, &full[s], kb * GK,
-                                  w.a_load_row, 0x3);
-          } else {
-            tma_load_2d(&maps.a128, a_dst, &full[s], kb * GK, w.a_load_row);
-          }
-          if (w.mode == 1) {
-            tma_load_2d_multicast(&maps.b_half, b_dst + rank * (BN / 2) * 128, &full[s], 0,
-                                  w.b_load_row + kb * BN, 0x3);
-          } else {
-            tma_load_2d(&maps.b_full, b_dst, &full[s], 0, w.b_load_row + kb * BN);
-          }
+          tma_load_2d(&maps.a128, sA + s * C::A_BYTES, &full[s], kb * GK, w.a_load_row);
+          tma_load_2d(&maps.b_tile, sB + s * C::B_BYTES, &full[s], 0, w.b_load_row + kb * BN);
         }
       }
       if (aborted) {
@@ -326,7 +274,7 @@ __global__ void __launch_bounds__(192, 1)
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t IDESC = idesc_bf16_f32(GM, BN);
       int it = 0, tcount = 0;
-      for (int u = unit0; u < total; u += unit_step, ++tcount) {
+      for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (!mbar_wait_bounded(&tempty[acc], aph ^ 1, abort_flag, status, spin_limit)) break;
@@ -349,8 +297,7 @@ __global__ void __launch_bounds__(192, 1)
                      sdesc_k_major_sw128(b_addr + kk * UK * 2), IDESC,
                      (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          if constexpr (CL == 2) mma_commit_multicast(&empty[s], 0x3);
-          else mma_commit(&empty[s]);
+          mma_commit(&empty[s]);
         }
         if (aborted) break;
         mma_commit(&tfull[acc]);
@@ -363,8 +310,8 @@ __global__ void __launch_bounds__(192, 1)
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int tcount = 0;
-    for (int u = unit0; u < total; u += unit_step, ++tcount) {
-      const Work w = decode<BN, CL>(u, rank, s_prefix, s_off, s_mt, E, NT, KB, a_local);
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
+      const Work w = decode<BN>(u, s_prefix, s_off, E, NT, KB, a_local);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       int ok = 1;
@@ -384,7 +331,6 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (CL == 2) cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -510,7 +456,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&maps.a128);
-    prefetch_tensormap(&maps.b_half);
+    prefetch_tensormap(&maps.b_tile);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
@@ -537,7 +483,7 @@ __global__ void __launch_bounds__(192, 1)
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
           const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
           tma_load_2d_pair(&maps.a128, sA + s * C::A_BYTES, bar, kb * GK, w.a_load_row);
-          tma_load_2d_pair(&maps.b_half, sB + s * C::B_BYTES, bar, 0, w.b_load_row + kb * BN);
+          tma_load_2d_pair(&maps.b_tile, sB + s * C::B_BYTES, bar, 0, w.b_load_row + kb * BN);
         }
       }
       if (aborted && rank == 0) {
@@ -615,9 +561,8 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-// Per device and kernel: the shared-memory opt-in and the grid (SMs, or twice
-// the number of co-resident two-CTA clusters).
-template <int BN, bool SWIGLU, int CL>
+// Per device and kernel: the shared-memory opt-in and the grid (one CTA per SM).
+template <int BN, bool SWIGLU>
 cudaError_t kernel_grid(int* grid) {
   using C = Cfg<BN>;
   static int cache[64] = {};
@@ -628,57 +573,26 @@ cudaError_t kernel_grid(int* grid) {
     *grid = cache[dev];
     return cudaSuccess;
   }
-  auto kern = grouped_gemm_kernel<BN, SWIGLU, CL>;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  err = cudaFuncSetAttribute(grouped_gemm_kernel<BN, SWIGLU>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  int g = device_sm_count();
-  if constexpr (CL == 2) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * g, 1, 1);
-    cfg.blockDim = dim3(192, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-    if (err != cudaSuccess) return err;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
-    g = 2 * clusters;
-  }
+  const int g = device_sm_count();
   if (dev < 64) cache[dev] = g;
   *grid = g;
   return cudaSuccess;
 }
 
-template <int BN, bool SWIGLU, int CL>
+template <int BN, bool SWIGLU>
 cudaError_t launch_grouped(const Maps& maps, const int32_t* offsets, int E, int R,
                            int n_per_expert, int K, void* out, int out_ld, int32_t* status,
-                           long long spin_limit, cudaStream_t s, int a_local = 0) {
+                           long long spin_limit, cudaStream_t s, int a_local) {
   using C = Cfg<BN>;
   int grid = 0;
-  cudaError_t err = kernel_grid<BN, SWIGLU, CL>(&grid);
+  cudaError_t err = kernel_grid<BN, SWIGLU>(&grid);
   if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = s;
-  if constexpr (CL == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<BN, SWIGLU, CL>, maps, offsets, E, R,
-                            n_per_expert, K, out, out_ld, status, spin_limit, a_local);
+  grouped_gemm_kernel<BN, SWIGLU><<<grid, 192, C::SMEM_BYTES, s>>>(
+      maps, offsets, E, R, n_per_expert, K, out, out_ld, status, spin_limit, a_local);
+  return cudaGetLastError();
 }
 
 // Grid of the pair kernel: twice the number of co-resident two-CTA clusters.
@@ -740,16 +654,15 @@ cudaError_t launch_pair(const Maps& maps, const int32_t* offsets, int E, int R, 
                             n_per_expert, K, out, out_ld, status, spin_limit, a_local);
 }
 
-// The pair kernel and the single-CTA kernel give the same bits for every row (the
-// same MMA shape per row, K order and epilogue), so the choice below may depend on
-// the number of rows without breaking batch invariance.  Measured on GB300: the
-// pair form is 2-8% faster for the down GEMM when experts hold many rows and K is
-// not short; it is slower for decode-sized experts (half of each stage's A rows are
-// empty) and for short K (both CTAs' epilogues gate every accumulator), and no
-// faster for the gate/up GEMM.
-bool use_pair_down(int E, int R, int I) { return I >= 768 && (long long)R >= 512LL * E; }
-
 }  // namespace
+
+// The pair kernel and the single-CTA kernel give the same bits for every row (the
+// same MMA shape per row, K order and epilogue), so the choice may depend on the
+// number of rows without breaking batch invariance.  The pair form halves each
+// SM's B traffic from L2 and shared memory; it pays when experts hold many rows
+// (few half-empty 256-row tiles) and K is not short (both CTAs' epilogues gate
+// every accumulator).
+bool use_pair_gemm(int E, int R, int K) { return K >= 768 && (long long)R >= 512LL * E; }
 
 int gemm_down_bn(int H) { return (H % 256 == 0) ? 256 : 128; }
 
@@ -757,16 +670,15 @@ cudaError_t launch_gemm_gate_up(const GemmOperand& a, const GemmOperand& b, cons
                                 int E, int R, int H, int I, void* h, int32_t* status,
                                 long long spin_limit, cudaStream_t s, bool a_local) {
   if (R == 0) return cudaSuccess;
+  const bool pair = use_pair_gemm(E, R, H);
   Maps m;
-  if (!a.encode(&m.a128, 128) || !a.encode(&m.a64, 64) || !b.encode(&m.b_full, 256) ||
-      !b.encode(&m.b_half, 128))
+  if (!a.encode(&m.a128, 128) || !b.encode(&m.b_tile, pair ? 128 : 256))
     return cudaErrorInvalidValue;
-  const int NT = (2 * I) / 256;
-  if (NT % 2 == 0)
-    return launch_grouped<256, true, 2>(m, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
-                                        a_local ? 1 : 0);
-  return launch_grouped<256, true, 1>(m, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
-                                      a_local ? 1 : 0);
+  if (pair)
+    return launch_pair<256, true>(m, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
+                                  a_local ? 1 : 0);
+  return launch_grouped<256, true>(m, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
+                                   a_local ? 1 : 0);
 }
 
 cudaError_t launch_gemm_down(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets,
@@ -774,24 +686,18 @@ cudaError_t launch_gemm_down(const GemmOperand& a, const GemmOperand& b, const i
                              long long spin_limit, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   const int bn = gemm_down_bn(H);
+  const bool pair = use_pair_gemm(E, R, I);
   Maps m;
-  if (!a.encode(&m.a128, 128) || !a.encode(&m.a64, 64) || !b.encode(&m.b_full, bn) ||
-      !b.encode(&m.b_half, bn / 2))
+  if (!a.encode(&m.a128, 128) || !b.encode(&m.b_tile, pair ? bn / 2 : bn))
     return cudaErrorInvalidValue;
-  const int NT = H / bn;
-  if (use_pair_down(E, R, I)) {
+  if (pair) {
     if (bn == 256)
       return launch_pair<256, false>(m, offsets, E, R, H, I, y, H, status, spin_limit, s, 0);
     return launch_pair<128, false>(m, offsets, E, R, H, I, y, H, status, spin_limit, s, 0);
   }
-  if (bn == 256) {
-    if (NT % 2 == 0)
-      return launch_grouped<256, false, 2>(m, offsets, E, R, H, I, y, H, status, spin_limit, s);
-    return launch_grouped<256, false, 1>(m, offsets, E, R, H, I, y, H, status, spin_limit, s);
-  }
-  if (NT % 2 == 0)
-    return launch_grouped<128, false, 2>(m, offsets, E, R, H, I, y, H, status, spin_limit, s);
-  return launch_grouped<128, false, 1>(m, offsets, E, R, H, I, y, H, status, spin_limit, s);
+  if (bn == 256)
+    return launch_grouped<256, false>(m, offsets, E, R, H, I, y, H, status, spin_limit, s, 0);
+  return launch_grouped<128, false>(m, offsets, E, R, H, I, y, H, status, spin_limit, s, 0);
 }
 
 }  // namespace moe

@@ -6,7 +6,16 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "moe.h"
+
 namespace moe {
+
+// Host-side argument checks of the C ABI (moe_api.cu), for entry points defined
+// in other translation units: dims within the library's limits, a non-null
+// 16-byte-aligned pointer, a current device that is sm_103.
+moe_status validate_dims(const moe_dims& d);
+moe_status validate_ptr(const void* p);
+moe_status validate_device();
 
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;

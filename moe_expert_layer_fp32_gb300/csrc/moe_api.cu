@@ -161,6 +161,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
+moe_status validate_dims(const moe_dims& d) { return check_dims(d); }
+moe_status validate_ptr(const void* p) { return need(p); }
+moe_status validate_device() { return device_ok(); }
+
 bool GemmOperand::encode(CUtensorMap* m, uint32_t box_rows) const {
   auto fn = encode_fn();
   if (fn == nullptr) return false;

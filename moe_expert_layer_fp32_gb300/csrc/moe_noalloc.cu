@@ -13,7 +13,10 @@
 // The scratch is the file-scope array below (2 MiB per GPU that loads the
 // library, held until the process exits).  Host code cannot use the array's
 // name as a device address: it is looked up once per device with
-// cudaGetSymbolAddress and that address is what the kernels receive.
+// cudaGetSymbolAddress and that address is what the kernels receive.  The cached
+// address belongs to the device's current context: after cudaDeviceReset on a
+// device, this entry point must not be called on that device again in the same
+// process.
 #include <mutex>
 
 #include "common.cuh"
@@ -53,14 +56,16 @@ using namespace moe;
 extern "C" moe_status moe_load_stats_noalloc(const int32_t* topk_idx, moe_dims d, int32_t* counts,
                                              int32_t* offsets, int32_t* device_status,
                                              void* stream) {
-  if (d.T < 0 || d.H <= 0 || d.E <= 0 || d.k <= 0 || d.I <= 0 || d.k > d.E)
-    return MOE_ERR_INVALID_ARG;
-  if (d.E > kMaxE || d.k > kMaxK || (long long)d.T * d.k >= (1LL << 31))
-    return MOE_ERR_UNSUPPORTED;
+  // the checks of moe_load_stats: dims, pointers (16-byte aligned), sm_103 device
+  moe_status st = validate_dims(d);
+  if (st != MOE_OK) return st;
   const long long nb = ((long long)d.T + kPermBlock - 1) / kPermBlock;
   if (2 * nb * d.E > (long long)kNoAllocScratchInts) return MOE_ERR_UNSUPPORTED;
-  if (counts == nullptr || offsets == nullptr || (d.T > 0 && topk_idx == nullptr))
-    return MOE_ERR_INVALID_ARG;
+  if (d.T > 0 && (st = validate_ptr(topk_idx)) != MOE_OK) return st;
+  if ((st = validate_ptr(counts)) != MOE_OK) return st;
+  if ((st = validate_ptr(offsets)) != MOE_OK) return st;
+  if (device_status != nullptr && (st = validate_ptr(device_status)) != MOE_OK) return st;
+  if ((st = validate_device()) != MOE_OK) return st;
   int32_t* scratch = scratch_on_current_device();
   if (scratch == nullptr) return MOE_ERR_CUDA;
   int32_t* blk_counts = scratch;

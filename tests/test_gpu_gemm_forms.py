@@ -1,4 +1,4 @@
-"""The two forms of the grouped expert GEMMs give the same bits.
+"""The three forms of the grouped expert GEMMs give the same bits.
 
   "0 train-infer mismatch for open-weight MoE RL", section "Matrix
   multiplication: the same reduction along K": a row's result must not depend
@@ -6,11 +6,12 @@
 
 The tile kernels put token rows on the MMA's M side (128 per tile); the swapped
 kernels, used for small batches, put weight rows on M and up to 64 token rows on
-N.  Both sum the same BF16 products in the same K order, so every row of h and y
-must be bit-identical.  moe_expert_ffn picks the form from the dims alone
-(moe_expert_ffn_form): the same expert rows are run once with few rows in total
-(swapped form) and once with many more rows added to the last expert (tile
-form), and the shared rows are compared bit for bit.
+N; the pair kernels, used from 512 rows per expert on average, run one M = 256
+MMA over two CTAs.  All of them sum the same BF16 products in the same K order,
+so every row of h and y must be bit-identical.  moe_expert_ffn picks the form
+from the dims alone (moe_expert_ffn_form): the same expert rows are run with few
+rows in total (swapped form), with more rows added to the last expert (single-CTA
+tiles) and with many more (pairs), and the shared rows are compared bit for bit.
 """
 import numpy as np
 import pytest
@@ -71,3 +72,24 @@ def test_swapped_and_tile_forms_bit_identical(moe, name):
     sub_off[1:] = np.cumsum(counts_small[experts])
     ref = oracle.expert_ffn(x[rows], sub_off, wg, wu, wd)
     assert_close_f32(y_small[rows], ref)
+
+
+@pytest.mark.parametrize("name", ["fine_grained", "packed_rl"])
+def test_single_cta_and_pair_forms_bit_identical(moe, name):
+    """Expert row counts around the 128- and 256-row tile edges (odd last tiles,
+    an expert whose rows end inside the odd CTA's half, empty experts): the same
+    rows through the single-CTA tile kernels (under 512 rows per expert on
+    average) and through the pair kernels (above) give the same bits."""
+    wl = synth.WORKLOADS[name]
+    W = weights(wl)
+    counts_mid = np.zeros(wl.E, dtype=np.int64)
+    edges = [1, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 640]
+    counts_mid[0:3 * len(edges):3] = edges
+    counts_mid[-1] = 5
+    R_mid = int(counts_mid.sum())
+    counts_big = counts_mid.copy()
+    counts_big[-1] += 512 * wl.E  # the last expert's first rows are shared
+    x = synth.tokens(wl, int(counts_big.sum()))
+    y_mid, _ = ffn(moe, wl, W, x, counts_mid, form=0)
+    y_big, _ = ffn(moe, wl, W, x, counts_big, form=0)
+    np.testing.assert_array_equal(y_mid.view(np.uint32), y_big[:R_mid].view(np.uint32))

@@ -121,8 +121,8 @@ def test_host_batches_pipeline_matches_device_calls(moe):
 
 @pytest.mark.parametrize("name", ["fine_grained", "packed_rl", "tiny"])
 def test_layer_equals_step_by_step_calls(moe, name):
-    """moe_layer_fwd (combine fused into the down GEMM) gives the same bytes as the
-    step-by-step ABI calls ending in the stand-alone moe_combine."""
+    """moe_layer_fwd gives the same bytes as the step-by-step ABI calls (route,
+    load stats, permute, expert FFN, combine) on the same inputs."""
     wl = synth.WORKLOADS[name]
     W = weights(wl)
     x = synth.tokens(wl)
@@ -152,9 +152,9 @@ def test_layer_equals_step_by_step_calls(moe, name):
 
 
 def test_batch_invariance_across_gemm_variants(cuda_ok):
-    """The down GEMM runs as a pair of CTAs (one M=256 MMA) from 512 rows per expert
-    on average, and as single CTAs below; the fine_grained layer crosses that line
-    between T = 4095 and T = 4096.  Each token's output must not change."""
+    """Both grouped GEMMs run as pairs of CTAs (one M=256 MMA) from 512 rows per
+    expert on average, and as single CTAs below; the fine_grained layer crosses that
+    line between T = 4095 and T = 4096.  Each token's output must not change."""
     import moe_expert_layer_fp32_gb300 as moe
     from gpu_util import weights
     wl = synth.WORKLOADS["fine_grained"]

@@ -1,8 +1,10 @@
 """moe_load_stats_noalloc: the load statistics for callers that cannot allocate
 device memory (its scratch is a fixed array inside the library rather than a
 caller workspace).  Called through the C ABI twice in a row on different inputs,
-its counts and offsets must equal those of moe_load_stats on the same inputs
-(bit-exact, like every integer output of the library), with no device-side error.
+its counts and offsets must equal those of moe_load_stats on the same inputs and
+those of the CPU oracle (bit-exact, like every integer output of the library),
+with no device-side error.  An empty batch gives all-zero counts and offsets, and
+a token that names one expert twice is reported through the device status word.
 
 This file is named to be collected last, so that a run stopping at the first
 failure has already run every other test."""
@@ -55,6 +57,32 @@ def test_noalloc_matches_workspace_version_twice(moe):
         np.testing.assert_array_equal(counts.cpu().numpy(), counts_ref.cpu().numpy())
         np.testing.assert_array_equal(offsets.cpu().numpy(), offsets_ref.cpu().numpy())
         assert int(offsets[-1].item()) == idx.size
+        counts_o, offsets_o, _, _ = oracle.load_stats(idx, wl.E)
+        np.testing.assert_array_equal(counts.cpu().numpy(), counts_o)
+        np.testing.assert_array_equal(offsets.cpu().numpy(), offsets_o)
+
+
+def test_noalloc_empty_batch_and_repeated_expert(moe):
+    E = 16
+    # T = 0: nothing to count; every count and offset is written as 0
+    d = moe.dims(0, 128, E, 2, 128)
+    counts = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+    offsets = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_load_stats_noalloc(torch.empty((0, 2), dtype=torch.int32, device="cuda"), d, counts,
+                               offsets, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert not counts.any().item() and not offsets.any().item()
+
+    # token 3 names expert 5 twice: flagged, never a silent count
+    idx = random_distinct_idx(300, E, 2, seed=9)
+    idx[3] = [5, 5]
+    d = moe.dims(300, 128, E, 2, 128)
+    status.zero_()
+    moe.moe_load_stats_noalloc(torch.from_numpy(idx).cuda(), d, counts, offsets, status)
+    torch.cuda.synchronize()
+    assert moe.STATUS[int(status.item())] == "MOE_ERR_DEVICE_CHECK"
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(moe):
