@@ -23,9 +23,14 @@
 // one MMA per half into two TMEM accumulators of N columns (double-buffered).
 // Units are numbered expert-major, then weight column, then token tile, so the
 // token tiles of one weight column run side by side and share its L2 lines.
-// For the down GEMM, when whole-box units would fill at most half of the SMs, a
-// unit is one 128-row half of a box (HV = 1): one MMA per K step, twice the
-// units, the same chain and epilogue per element.
+// When whole-box units would fill at most half of the SMs, units shrink so that
+// twice as many SMs stream the weights, with the same chain and epilogue per
+// element:
+//   down (HV = 1): one 128-row half of a box, one MMA per K step;
+//   gate/up (HV = 4): 64 gate rows and the matching 64 up rows of a box, loaded
+//     as two 64-row boxes into one 128-row operand, one MMA per K step; TMEM
+//     lanes 0-63 then hold gate and 64-127 up, so the two epilogue warps that own
+//     the up lanes pass their values to the gate warps through shared memory.
 //
 // Each output element is the same K order (64-wide k-blocks ascending, 16-wide
 // MMAs ascending, FP32 accumulation from zero) over the same BF16 products as in
@@ -54,23 +59,27 @@ constexpr int HALF = 128;                    // MMA M
 constexpr int TT = 64;                       // token rows per unit at most (MMA N <= 64)
 constexpr int X_BYTES = TT * SK * 2;         // 8 KB (N = 64)
 
-// HV halves of a packed box per unit: 2 (a whole box; gate and up must meet in one
-// CTA) or 1 (one 128-row half: twice the units, for the down GEMM when whole-box
-// units would leave most SMs idle).
+// HV selects the unit: 2 = a whole packed box (two M = 128 MMAs per K step; gate
+// and up meet in one CTA), 1 = one 128-row half of a box (down only), 4 = 64 gate
+// rows + the matching 64 up rows of a box in one M = 128 operand (gate/up only).
 template <int HV>
 struct SwapCfg {
-  static constexpr int UROWS = HALF * HV;              // weight rows per unit
+  static constexpr int UROWS = HV == 2 ? 2 * HALF : HALF;  // weight rows per unit
+  static constexpr int NMMA = HV == 2 ? 2 : 1;             // M = 128 MMAs per K step
   static constexpr int STAGES = HV == 2 ? 5 : 8;
-  static constexpr int W_BYTES = UROWS * SK * 2;       // 32 or 16 KB
-  static constexpr int ACC_COLS = HV * TT;             // one accumulator buffer
-  static constexpr int TMEM_COLS = 2 * ACC_COLS;       // double-buffered
+  static constexpr int W_BYTES = UROWS * SK * 2;           // 32 or 16 KB
+  static constexpr int ACC_COLS = NMMA * TT;               // one accumulator buffer
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;           // double-buffered
   static constexpr int NBAR = 2 * STAGES + 2 + 2 + 1;
-  static constexpr int SMEM_BYTES =
-      1024 + STAGES * (W_BYTES + X_BYTES) + NBAR * 8 + 16 + 3 * (kMaxE + 1) * 4;
+  // HV = 4: up values of 64 weight rows x 64 token rows, passed to the gate warps
+  static constexpr int XCH_BYTES = HV == 4 ? 64 * (TT + 1) * 4 : 0;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * (W_BYTES + X_BYTES) + XCH_BYTES + NBAR * 8 +
+                                    16 + 3 * (kMaxE + 1) * 4;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
-// Weight boxes (256 rows) and token boxes of 16, 32 and 64 rows; all 64 columns.
+// Weight boxes (UROWS rows; 64 for HV = 4) and token boxes of 16, 32 and 64 rows;
+// all 64 columns.
 struct SwapMaps {
   CUtensorMap w, x16, x32, x64;
 };
@@ -104,9 +113,14 @@ __device__ __forceinline__ SwapWork swap_decode(int u, const int* s_prefix, cons
   w.rows = min(TT, s_off[lo + 1] - w.row0);
   w.nb = w.rows <= 16 ? 16 : (w.rows <= 32 ? 32 : 64);
   w.x_load_row = w.row0 - (a_local ? s_off[lo] : 0);
-  // box row of (expert, box column, k-block 0), plus the half within the box
-  const int NTB = NTW * HV / 2;  // packed boxes per expert
-  w.w_load_row = (lo * NTB + (w.wt * HV >> 1)) * KB * WROWS + (HV == 1 ? (w.wt & 1) * HALF : 0);
+  // box row of (expert, box, k-block 0), plus the unit's rows within the box:
+  // HV = 1 its 128-row half, HV = 4 its 64 gate rows (its up rows are 128 further)
+  if constexpr (HV == 2) {
+    w.w_load_row = (lo * NTW + w.wt) * KB * WROWS;
+  } else {
+    const int NTB = NTW / 2;  // packed boxes per expert
+    w.w_load_row = (lo * NTB + (w.wt >> 1)) * KB * WROWS + (w.wt & 1) * (HV == 1 ? HALF : 64);
+  }
   return w;
 }
 
@@ -129,14 +143,15 @@ __global__ void __launch_bounds__(192, 1)
                              int K, void* __restrict__ out, int out_ld, int32_t* status,
                              long long spin_limit, int a_local) {
   using C = SwapCfg<HV>;
-  static_assert(!SWIGLU || HV == 2, "gate and up rows of a unit must meet in one CTA");
+  static_assert(SWIGLU ? HV != 1 : HV != 4, "gate and up rows of a unit must meet in one CTA");
   constexpr int STAGES = C::STAGES, W_BYTES = C::W_BYTES, ACC_COLS = C::ACC_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sW = base;
   uint8_t* sX = base + STAGES * W_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sX + STAGES * X_BYTES);
+  float* s_xch = reinterpret_cast<float*>(sX + STAGES * X_BYTES);  // HV = 4 only
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sX + STAGES * X_BYTES + C::XCH_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -215,6 +230,9 @@ __global__ void __launch_bounds__(192, 1)
           }
           mbar_arrive_expect_tx(&full[s], bytes);
           tma_load_2d(&maps.w, sW + s * W_BYTES, &full[s], 0, w.w_load_row + kb * WROWS);
+          if constexpr (HV == 4)  // the matching up rows, into operand rows 64..127
+            tma_load_2d(&maps.w, sW + s * W_BYTES + 64 * 128, &full[s], 0,
+                        w.w_load_row + HALF + kb * WROWS);
           tma_load_2d(xm, sX + s * X_BYTES, &full[s], kb * SK, w.x_load_row);
         }
       }
@@ -275,10 +293,43 @@ __global__ void __launch_bounds__(192, 1)
       int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(&tfull[acc], aph, abort_flag, status, spin_limit);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      // HV = 4: the four warps meet at barriers below, so they go on or stop together
+      if constexpr (HV == 4) ok = named_barrier_and(1, 128, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-      if constexpr (SWIGLU) {
+      if constexpr (HV == 4) {
+        // lanes 0-63: gate, 64-127: up, of intermediate column wt * 64 + (lane % 64);
+        // warps owning the up lanes (q = 2, 3) hand them to the gate warps (q = 0, 1)
+        float* xr = s_xch + (q & 1) * 32 * (TT + 1) + lane * (TT + 1);
+        if (q >= 2) {
+          for (int j0 = 0; j0 < w.nb; j0 += 16) {
+            uint32_t uu[16];
+            tmem_ld_32x32b_x16(taddr + j0, uu);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) xr[j0 + i] = __uint_as_float(uu[i]);
+          }
+        }
+        named_barrier_sync(1, 128);
+        if (q < 2) {
+          uint16_t* h = static_cast<uint16_t*>(out) + (size_t)w.wt * 64 + q * 32 + lane;
+          for (int j0 = 0; j0 < w.nb; j0 += 16) {
+            uint32_t g[16];
+            tmem_ld_32x32b_x16(taddr + j0, g);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = j0 + i;
+              if (j < w.rows) {
+                const float hv = __fmul_rn(silu_f32(__uint_as_float(g[i])), xr[j]);
+                h[(size_t)(w.row0 + j) * out_ld] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+              }
+            }
+          }
+        }
+        named_barrier_sync(1, 128);  // the exchange buffer is free for the next unit
+      } else if constexpr (SWIGLU) {
         // half 0: gate, half 1: up, of intermediate column wt * 128 + 32 q + lane
         uint16_t* h = static_cast<uint16_t*>(out) + (size_t)w.wt * HALF + q * 32 + lane;
         for (int j0 = 0; j0 < w.nb; j0 += 16) {
@@ -297,10 +348,10 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       } else {
-        // half c: output columns wt * 256 + 128 c + 32 q + lane
+        // half c: output columns wt * UROWS + 128 c + 32 q + lane
         float* y = static_cast<float*>(out) + (size_t)w.wt * C::UROWS + q * 32 + lane;
 #pragma unroll
-        for (int c = 0; c < HV; ++c) {
+        for (int c = 0; c < C::NMMA; ++c) {
           for (int j0 = 0; j0 < w.nb; j0 += 16) {
             uint32_t v[16];
             tmem_ld_32x32b_x16(taddr + c * TT + j0, v);
@@ -332,7 +383,7 @@ cudaError_t launch_swap(const GemmOperand& a, const GemmOperand& b, const int32_
                         long long spin_limit, cudaStream_t s, int a_local) {
   SwapMaps m;
   using C = SwapCfg<HV>;
-  if (!b.encode(&m.w, C::UROWS) || !a.encode(&m.x16, 16) || !a.encode(&m.x32, 32) ||
+  if (!b.encode(&m.w, HV == 4 ? 64 : C::UROWS) || !a.encode(&m.x16, 16) || !a.encode(&m.x32, 32) ||
       !a.encode(&m.x64, TT))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
@@ -374,6 +425,12 @@ cudaError_t launch_gemm_gate_up_swap(const GemmOperand& a, const GemmOperand& b,
                                      int32_t* status, long long spin_limit, cudaStream_t s,
                                      bool a_local) {
   if (R == 0) return cudaSuccess;
+  // quarter units (64 gate + 64 up rows) while whole-box units would fill at most
+  // half of the SMs (experts with rows <= min(E, R)); each element's chain and
+  // epilogue arithmetic are the same
+  if (2LL * (2 * I / WROWS) * std::min(E, R) <= device_sm_count())
+    return launch_swap<true, 4>(a, b, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
+                                a_local ? 1 : 0);
   return launch_swap<true, 2>(a, b, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
                            a_local ? 1 : 0);
 }

@@ -45,22 +45,14 @@ constexpr int BT = 32;       // tokens per CTA (large-T kernel)
 constexpr int NTHR = 128;
 constexpr int NST = 3;       // cp.async ring depth
 
-// Inner-loop form of the large-T kernels: 0 = one FFMA per logit per hidden row;
-// 1 = packed FFMA2 (two experts' chains per instruction), token values paired in
-// registers; 2 = packed FFMA2 with every token value stored twice in the widened
-// x chunk, so each 16-byte load yields two ready pairs.  Each lane of an FFMA2 is
-// the same IEEE round-to-nearest fused multiply-add as fmaf, so every logit is
-// the same chain in every form.
-constexpr int kRouteForm = 2;
-constexpr int XDUP = kRouteForm == 2 ? 2 : 1;  // copies of each token value in xs
-constexpr int XLD = XDUP * BT + 4;             // row stride of the transposed FP32 x chunk
+constexpr int XLD = BT + 4;  // row stride of the transposed FP32 x chunk
 
 template <int EP>
 struct RouteCfg {
   static constexpr int HK = (2048 / EP > 16) ? 2048 / EP : 16;  // 8-16 KB of W_r per chunk
   static constexpr int w_floats = NST * HK * EP;        // W_r ring
   static constexpr int xst_halves = NST * BT * HK;      // bf16 x ring
-  static constexpr int xs_floats = HK * XLD;            // FP32 transposed x (XDUP copies)
+  static constexpr int xs_floats = HK * XLD;            // FP32 transposed x
   static constexpr int ring_bytes = 4 * w_floats + 2 * xst_halves + 4 * xs_floats;
   static constexpr int logit_bytes = 4 * BT * (EP + 1);
   static constexpr int bytes = ring_bytes > logit_bytes ? ring_bytes : logit_bytes;
@@ -100,7 +92,14 @@ __device__ __forceinline__ float exp_cw(float x) {
   return ldexpf(p, (int)n);
 }
 
-// acc[i][2p], acc[i][2p+1] += x[i] * (w[2p], w[2p+1]): per lane one IEEE RN fma.
+// The large-T kernels advance two experts' chains per instruction: FFMA2 on
+// (x, x) * (w_e, w_e+1) + (acc_e, acc_e+1).  Each lane is the same IEEE
+// round-to-nearest fused multiply-add as fmaf, so every logit is the same chain
+// as one FFMA per step would give; the packed form halves the FMA issue slots of
+// these issue-bound loops.  Measured on GB300 (router stage): large 1.59 -> 1.43-
+// 1.47 ms, packed_rl 255 -> 236 us, ling3_tiny 198 -> 186 us, fine_grained T = 4096
+// 73 -> 70 us.  Storing every token value twice in shared memory, so a 16-byte
+// load gives two ready pairs, was slower than either (large 1.71 ms).
 __device__ __forceinline__ float2 ffma2(float2 x, float2 w, float2 acc) {
   return __ffma2_rn(x, w, acc);
 }
@@ -234,33 +233,14 @@ __device__ __forceinline__ void route_one_token(const float* lrow, const float* 
   }
 }
 
-// One widened token value into the transposed x chunk (XDUP copies side by side).
-__device__ __forceinline__ void store_x(float* dst, float v) {
-  if constexpr (XDUP == 2) *reinterpret_cast<float2*>(dst) = make_float2(v, v);
-  else *dst = v;
-}
-
-// Eight token values of one hidden row as (x, x) pairs: two runs of four tokens,
-// `gap` tokens apart.  With XDUP == 2 each pair is two adjacent stored copies, so
-// a 16-byte load gives two pairs ready for FFMA2 without register moves.
+// Eight token values of one hidden row as (x, x) pairs for FFMA2: two runs of
+// four tokens, `gap` tokens apart in the transposed x chunk.
 __device__ __forceinline__ void load_x8(const float* src, int gap, float2 (&xp)[8]) {
-  if constexpr (XDUP == 2) {
+  const float4 a = *reinterpret_cast<const float4*>(src);
+  const float4 b = *reinterpret_cast<const float4*>(src + gap);
+  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float4 a = *reinterpret_cast<const float4*>(src + 2 * gap * h);
-      const float4 b = *reinterpret_cast<const float4*>(src + 2 * gap * h + 4);
-      xp[4 * h + 0] = make_float2(a.x, a.y);
-      xp[4 * h + 1] = make_float2(a.z, a.w);
-      xp[4 * h + 2] = make_float2(b.x, b.y);
-      xp[4 * h + 3] = make_float2(b.z, b.w);
-    }
-  } else {
-    const float4 a = *reinterpret_cast<const float4*>(src);
-    const float4 b = *reinterpret_cast<const float4*>(src + gap);
-    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) xp[i] = make_float2(v[i], v[i]);
-  }
+  for (int i = 0; i < 8; ++i) xp[i] = make_float2(v[i], v[i]);
 }
 
 template <int EP, int KIND>
@@ -335,21 +315,21 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
     issue_chunk(c + NST - 1);
     cp_async_wait<NST - 1>();
     __syncthreads();
-    // widen the x chunk to FP32, transposed: xs[h][token] (XDUP copies each)
+    // widen the x chunk to FP32, transposed: xs[h][token]
     for (int i = tid; i < BT * HK / 4; i += NTHR) {
       const int r = i / (HK / 4), hq = (i % (HK / 4)) * 4;
       const uint2 v = *reinterpret_cast<const uint2*>(xst + buf * BT * HK + r * HK + hq);
-      store_x(xs + (hq + 0) * XLD + XDUP * r, bf16_lo(v.x));
-      store_x(xs + (hq + 1) * XLD + XDUP * r, bf16_hi(v.x));
-      store_x(xs + (hq + 2) * XLD + XDUP * r, bf16_lo(v.y));
-      store_x(xs + (hq + 3) * XLD + XDUP * r, bf16_hi(v.y));
+      xs[(hq + 0) * XLD + r] = bf16_lo(v.x);
+      xs[(hq + 1) * XLD + r] = bf16_hi(v.x);
+      xs[(hq + 2) * XLD + r] = bf16_lo(v.y);
+      xs[(hq + 3) * XLD + r] = bf16_hi(v.y);
     }
     __syncthreads();
     const float* wsb = ws + buf * HK * EP;
 #pragma unroll 8
     for (int hh = 0; hh < HK; ++hh) {
       float2 xp[TT];
-      load_x8(xs + hh * XLD + XDUP * warp * TT, 4, xp);
+      load_x8(xs + hh * XLD + warp * TT, 4, xp);
       float wv[TE];
       if constexpr (TE >= 4) {
 #pragma unroll
@@ -367,11 +347,9 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
       } else {
         wv[0] = wsb[hh * EP + lane];
       }
-      if constexpr (kRouteForm == 0 || TE == 1) {
+      if constexpr (TE == 1) {
 #pragma unroll
-        for (int i = 0; i < TT; ++i)
-#pragma unroll
-          for (int j = 0; j < TE; ++j) acc[i][j] = fmaf(xp[i].x, wv[j], acc[i][j]);
+        for (int i = 0; i < TT; ++i) acc[i][0] = fmaf(xp[i].x, wv[0], acc[i][0]);
       } else {
 #pragma unroll
         for (int i = 0; i < TT; ++i) {
@@ -428,7 +406,7 @@ template <int EP>
 struct TileCfg {
   static constexpr int BT = 8192 / EP;
   static constexpr int HK = (EP >= 256) ? 16 : 32;
-  static constexpr int XL = XDUP * BT + 4;
+  static constexpr int XL = BT + 4;
   static constexpr int LE = (EP / 8 < 8) ? EP / 8 : 8;  // lanes along experts
   static constexpr int LT = 32 / LE;                    // lanes along tokens
   static constexpr int WE = (EP / 8) / LE;              // warps along experts
@@ -515,36 +493,28 @@ __global__ void __launch_bounds__(NTHR, 4) route_tile_kernel(const uint16_t* __r
     for (int i = tid; i < BTT * HK / 4; i += NTHR) {
       const int r = i / (HK / 4), hq = (i % (HK / 4)) * 4;
       const uint2 v = *reinterpret_cast<const uint2*>(xst + buf * BTT * HK + r * HK + hq);
-      store_x(xs + (hq + 0) * XL + XDUP * r, bf16_lo(v.x));
-      store_x(xs + (hq + 1) * XL + XDUP * r, bf16_hi(v.x));
-      store_x(xs + (hq + 2) * XL + XDUP * r, bf16_lo(v.y));
-      store_x(xs + (hq + 3) * XL + XDUP * r, bf16_hi(v.y));
+      xs[(hq + 0) * XL + r] = bf16_lo(v.x);
+      xs[(hq + 1) * XL + r] = bf16_hi(v.x);
+      xs[(hq + 2) * XL + r] = bf16_lo(v.y);
+      xs[(hq + 3) * XL + r] = bf16_hi(v.y);
     }
     __syncthreads();
     const float* wsb = ws + buf * HK * EP;
 #pragma unroll 4
     for (int hh = 0; hh < HK; ++hh) {
       float2 xp[8];
-      load_x8(xs + hh * XL + XDUP * tb, 4 * LT, xp);
+      load_x8(xs + hh * XL + tb, 4 * LT, xp);
       const float4 wa = *reinterpret_cast<const float4*>(wsb + hh * EP + eb);
       const float4 wb = *reinterpret_cast<const float4*>(wsb + hh * EP + eb + 4 * LE);
-      if constexpr (kRouteForm == 0) {
-        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      const float2 wp[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w),
+                            make_float2(wb.x, wb.y), make_float2(wb.z, wb.w)};
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xp[i].x, wv[j], acc[i][j]);
-      } else {
-        const float2 wp[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w),
-                              make_float2(wb.x, wb.y), make_float2(wb.z, wb.w)};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const float2 r = ffma2(xp[i], wp[p], make_float2(acc[i][2 * p], acc[i][2 * p + 1]));
-            acc[i][2 * p] = r.x;
-            acc[i][2 * p + 1] = r.y;
-          }
+        for (int p = 0; p < 4; ++p) {
+          const float2 r = ffma2(xp[i], wp[p], make_float2(acc[i][2 * p], acc[i][2 * p + 1]));
+          acc[i][2 * p] = r.x;
+          acc[i][2 * p + 1] = r.y;
         }
       }
     }

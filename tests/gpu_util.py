@@ -12,6 +12,31 @@ MAX_ABS = 2e-2
 REL_L2 = 5e-3
 
 
+def routing_weight_rtol(k: int) -> float:
+    """Relative bound on |w_gpu - w_oracle| for the softmax router's weights.
+
+    Both sides compute w_j = p_j / S with p_j = exp(l_j - m) / Z and S the left-to-
+    right sum of the k selected p.  The logits, m and l_j - m are the same bits on
+    both sides.  Z cancels out of the ratio up to the rounding of each p_j, so
+    its summation order (lane sums and an xor butterfly on the GPU, ascending on
+    the host) does not enter the bound.  With u = 2^-24 (half an ulp, relative), the
+    CUDA expf within 2 ulp (4u) and the host exp within 1 ulp (2u), each side's w_j
+    is within (e_j + e_max + (k - 1) + 1) u of the exact ratio, where e = exp error
+    + the division by Z: GPU (4+1)+(4+1)+k = k + 10, host (2+1)+(2+1)+k = k + 6.
+    The two sides differ by at most (2k + 16) u: 1.9e-6 for k = 8, 2.9e-6 for
+    k = 16."""
+    return (2 * k + 16) * 2.0 ** -24
+
+
+def assert_routing_weights_close(w: np.ndarray, w_ref: np.ndarray, k: int) -> None:
+    w = np.asarray(w, dtype=np.float64)
+    w_ref = np.asarray(w_ref, dtype=np.float64)
+    bound = routing_weight_rtol(k) * np.abs(w_ref)
+    err = np.abs(w - w_ref)
+    worst = float((err / np.maximum(np.abs(w_ref), 1e-300)).max()) if err.size else 0.0
+    assert np.all(err <= bound), f"routing weight rel. error {worst:.3e} > {routing_weight_rtol(k):.3e}"
+
+
 def dev_bf16(u16: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).cuda().view(torch.bfloat16)
 

@@ -8,7 +8,8 @@ import torch
 
 import oracle
 import synth
-from gpu_util import DeviceWeights, weights, assert_close, bits, dev, dev_bf16
+from gpu_util import (DeviceWeights, assert_close, assert_routing_weights_close, bits, dev,
+                      dev_bf16, weights)
 
 pytestmark = pytest.mark.gpu
 
@@ -70,7 +71,7 @@ def test_single_expert_is_dense_ffn(moe):
 def test_k_equals_E(moe):
     wl = synth.Workload("all", T=130, H=128, E=8, k=8, I=128, w_std=0.05)
     w, w_o = layer_vs_oracle(moe, wl)
-    np.testing.assert_allclose(w, w_o, rtol=4e-6, atol=1e-7)
+    assert_routing_weights_close(w, w_o, wl.k)
 
 
 def test_max_experts_and_k(moe):

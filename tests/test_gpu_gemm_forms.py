@@ -93,3 +93,27 @@ def test_single_cta_and_pair_forms_bit_identical(moe, name):
     y_mid, _ = ffn(moe, wl, W, x, counts_mid, form=0)
     y_big, _ = ffn(moe, wl, W, x, counts_big, form=0)
     np.testing.assert_array_equal(y_mid.view(np.uint32), y_big[:R_mid].view(np.uint32))
+
+
+@pytest.mark.parametrize("name", ["fine_grained", "ling3_tiny"])
+def test_quarter_and_half_box_units_bit_identical(moe, name):
+    """Decode-sized batches (at most a few experts with rows): the swapped gate/up
+    GEMM splits each packed box into 64-gate + 64-up-row units and the down GEMM
+    into 128-row halves.  Those rows must equal the tile kernels' bits."""
+    wl = synth.WORKLOADS[name]
+    W = weights(wl)
+    counts_small = np.zeros(wl.E, dtype=np.int64)
+    counts_small[[0, 5, 17, wl.E - 1]] = [1, 2, 3, 2]  # 8 rows in 4 experts
+    R_small = int(counts_small.sum())
+    counts_big = counts_small.copy()
+    counts_big[-1] += 64 * wl.E
+    x = synth.tokens(wl, int(counts_big.sum()))
+    y_small, offs = ffn(moe, wl, W, x, counts_small, form=1)
+    y_big, _ = ffn(moe, wl, W, x, counts_big, form=0)
+    np.testing.assert_array_equal(y_small.view(np.uint32), y_big[:R_small].view(np.uint32))
+    experts = np.nonzero(counts_small)[0]
+    wg, wu, wd = synth.expert_weights(wl, experts)
+    sub_off = np.zeros(len(experts) + 1, dtype=np.int32)
+    sub_off[1:] = np.cumsum(counts_small[experts])
+    ref = oracle.expert_ffn(x[:R_small], sub_off, wg, wu, wd)
+    assert_close_f32(y_small, ref)

@@ -13,7 +13,8 @@ import torch
 
 import oracle
 import synth
-from gpu_util import DeviceWeights, weights, assert_close, bits, dev, dev_bf16
+from gpu_util import (DeviceWeights, assert_close, assert_routing_weights_close, bits, dev,
+                      dev_bf16, weights)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +47,7 @@ def test_layer_matches_oracle(moe, name, sample):
     out, idx, w, counts = run_layer(moe, wl, W, x, wr, bias)
     idx_o, w_o = oracle.route(x, wr, bias, wl.k)
     np.testing.assert_array_equal(idx, idx_o)
-    np.testing.assert_allclose(w, w_o, rtol=4e-6, atol=1e-7)
+    assert_routing_weights_close(w, w_o, wl.k)
     counts_o, _, _, _ = oracle.load_stats(idx_o, wl.E)
     np.testing.assert_array_equal(counts, counts_o)
     if sample is None:

@@ -14,7 +14,8 @@ import torch
 
 import oracle
 import synth
-from gpu_util import DeviceWeights, weights, assert_close_f32, bits, dev, dev_bf16
+from gpu_util import (DeviceWeights, assert_close_f32, assert_routing_weights_close, bits, dev,
+                      dev_bf16, weights)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +47,7 @@ def test_route(moe, case):
     bias = None if case["bias"] is None else dev(case["bias"])
     moe.moe_route(dev_bf16(case["x"]), dev(case["wr"]), bias, d, idx, w)
     np.testing.assert_array_equal(idx.cpu().numpy(), case["idx"])
-    np.testing.assert_allclose(w.cpu().numpy(), case["w"], rtol=4e-6, atol=1e-7)
+    assert_routing_weights_close(w.cpu().numpy(), case["w"], wl.k)
 
 
 def test_load_stats(moe, case):
