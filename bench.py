@@ -55,8 +55,8 @@ METRIC = "routed tokens/s per MoE layer fwd"
 # one ncu capture of the same kernel on large-shaped rows at one eighth of the
 # size (E = 32 experts, T = 4096 tokens: the same 1024 rows per expert, H and I),
 # scaled by 8, the ratio of both the rows and the expert weights.  Valid while
-# the kernel sources are unchanged since the capture; None until it is taken.
-GEMM_TRAFFIC_LARGE = None
+# the kernel sources are unchanged since the capture.
+GEMM_TRAFFIC_LARGE = {"bytes": 8 * (1590218752 + 130554368), "sources_sha256_16": "539c1844104690c6"}
 
 
 def gemm_sources_hash():
