@@ -17,8 +17,8 @@
 // else EP/32 consecutive).  Chunks of HK = max(2048/EP, 16) hidden columns (8-16
 // KB of W_r) and the matching x columns are copied by cp.async into a 3-stage
 // ring while earlier chunks are multiplied (four CTAs fit on an SM); x is widened
-// once to FP32 into a transposed buffer, so a warp's eight token values for one h
-// are two broadcast loads.
+// once to FP32 into a transposed buffer (two of them, so each chunk costs two CTA
+// barriers), and a warp's eight token values for one h are two broadcast loads.
 //
 // route_cluster_kernel (T <= 1024): a cluster of eight CTAs (sixteen for T <= 8
 // and 64 experts or more) per 1, 2, 4 or 8 tokens, each CTA owning its share of
@@ -52,7 +52,7 @@ struct RouteCfg {
   static constexpr int HK = (2048 / EP > 16) ? 2048 / EP : 16;  // 8-16 KB of W_r per chunk
   static constexpr int w_floats = NST * HK * EP;        // W_r ring
   static constexpr int xst_halves = NST * BT * HK;      // bf16 x ring
-  static constexpr int xs_floats = HK * XLD;            // FP32 transposed x
+  static constexpr int xs_floats = 2 * HK * XLD;        // FP32 transposed x, two chunks
   static constexpr int ring_bytes = 4 * w_floats + 2 * xst_halves + 4 * xs_floats;
   static constexpr int logit_bytes = 4 * BT * (EP + 1);
   static constexpr int bytes = ring_bytes > logit_bytes ? ring_bytes : logit_bytes;
@@ -312,24 +312,27 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
   for (int c = 0; c < NST - 1; ++c) issue_chunk(c);
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c % NST;
-    issue_chunk(c + NST - 1);
-    cp_async_wait<NST - 1>();
+    // chunk c has landed; every thread is past chunk c-1, so its ring slot is free
+    cp_async_wait<NST - 2>();
     __syncthreads();
-    // widen the x chunk to FP32, transposed: xs[h][token]
+    issue_chunk(c + NST - 1);
+    // widen the x chunk to FP32, transposed: xsc[h][token] (two buffers: chunk c-1's
+    // may still be read by other warps)
+    float* xsc = xs + (c & 1) * HK * XLD;
     for (int i = tid; i < BT * HK / 4; i += NTHR) {
       const int r = i / (HK / 4), hq = (i % (HK / 4)) * 4;
       const uint2 v = *reinterpret_cast<const uint2*>(xst + buf * BT * HK + r * HK + hq);
-      xs[(hq + 0) * XLD + r] = bf16_lo(v.x);
-      xs[(hq + 1) * XLD + r] = bf16_hi(v.x);
-      xs[(hq + 2) * XLD + r] = bf16_lo(v.y);
-      xs[(hq + 3) * XLD + r] = bf16_hi(v.y);
+      xsc[(hq + 0) * XLD + r] = bf16_lo(v.x);
+      xsc[(hq + 1) * XLD + r] = bf16_hi(v.x);
+      xsc[(hq + 2) * XLD + r] = bf16_lo(v.y);
+      xsc[(hq + 3) * XLD + r] = bf16_hi(v.y);
     }
     __syncthreads();
     const float* wsb = ws + buf * HK * EP;
 #pragma unroll 8
     for (int hh = 0; hh < HK; ++hh) {
       float2 xp[TT];
-      load_x8(xs + hh * XLD + warp * TT, 4, xp);
+      load_x8(xsc + hh * XLD + warp * TT, 4, xp);
       float wv[TE];
       if constexpr (TE >= 4) {
 #pragma unroll
@@ -363,9 +366,9 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
         }
       }
     }
-    __syncthreads();
   }
   cp_async_wait<0>();
+  __syncthreads();  // the logits below overwrite the ring
 
   // ---- epilogue: logits (+ bias for the softmax router) to shared memory ---
   constexpr int LLD = EP + 1;
@@ -414,7 +417,7 @@ struct TileCfg {
   static_assert(WT * LT * 8 == BT, "tile");
   static constexpr int w_floats = NST * HK * EP;
   static constexpr int xst_halves = NST * BT * HK;
-  static constexpr int xs_floats = HK * XL;
+  static constexpr int xs_floats = 2 * HK * XL;  // two widened chunks
   static constexpr int ring_bytes = 4 * w_floats + 2 * xst_halves + 4 * xs_floats;
   static constexpr int logit_bytes = 4 * BT * (EP + 1);
   static constexpr int bytes = ring_bytes > logit_bytes ? ring_bytes : logit_bytes;
@@ -487,23 +490,25 @@ __global__ void __launch_bounds__(NTHR, 4) route_tile_kernel(const uint16_t* __r
   for (int c = 0; c < NST - 1; ++c) issue_chunk(c);
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c % NST;
-    issue_chunk(c + NST - 1);
-    cp_async_wait<NST - 1>();
+    // chunk c has landed; every thread is past chunk c-1, so its ring slot is free
+    cp_async_wait<NST - 2>();
     __syncthreads();
+    issue_chunk(c + NST - 1);
+    float* xsc = xs + (c & 1) * HK * XL;  // two widened chunks (see route_kernel)
     for (int i = tid; i < BTT * HK / 4; i += NTHR) {
       const int r = i / (HK / 4), hq = (i % (HK / 4)) * 4;
       const uint2 v = *reinterpret_cast<const uint2*>(xst + buf * BTT * HK + r * HK + hq);
-      xs[(hq + 0) * XL + r] = bf16_lo(v.x);
-      xs[(hq + 1) * XL + r] = bf16_hi(v.x);
-      xs[(hq + 2) * XL + r] = bf16_lo(v.y);
-      xs[(hq + 3) * XL + r] = bf16_hi(v.y);
+      xsc[(hq + 0) * XL + r] = bf16_lo(v.x);
+      xsc[(hq + 1) * XL + r] = bf16_hi(v.x);
+      xsc[(hq + 2) * XL + r] = bf16_lo(v.y);
+      xsc[(hq + 3) * XL + r] = bf16_hi(v.y);
     }
     __syncthreads();
     const float* wsb = ws + buf * HK * EP;
 #pragma unroll 4
     for (int hh = 0; hh < HK; ++hh) {
       float2 xp[8];
-      load_x8(xs + hh * XL + tb, 4 * LT, xp);
+      load_x8(xsc + hh * XL + tb, 4 * LT, xp);
       const float4 wa = *reinterpret_cast<const float4*>(wsb + hh * EP + eb);
       const float4 wb = *reinterpret_cast<const float4*>(wsb + hh * EP + eb + 4 * LE);
       const float2 wp[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w),
@@ -518,9 +523,9 @@ __global__ void __launch_bounds__(NTHR, 4) route_tile_kernel(const uint16_t* __r
         }
       }
     }
-    __syncthreads();
   }
   cp_async_wait<0>();
+  __syncthreads();  // the logits below overwrite the ring
 
   constexpr int LLD = EP + 1;
   const bool add_bias = KIND == 0 && bias != nullptr;
