@@ -249,9 +249,14 @@ __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, void* s
       : "memory");
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (this CTA's or the peer's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or the
+// peer's), with CTA-scope release.  Used to hand a drained TMEM accumulator back to
+// the pair's MMA thread: the tcgen05.ld reads are complete (tcgen05.wait::ld) and
+// ordered by tcgen05.fence::before_thread_sync, and nothing else the arriving warp
+// wrote is read by the MMA side, so a cluster-scope release (which would first wait
+// for the warp's global stores of its output rows to be performed) is not needed.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                : "memory");
 }
 

@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(192, 1)
                                  s_epi + q * 32 * C::EPI_LD, lane, out, out_ld);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
     }
   }
 

@@ -171,3 +171,47 @@ def test_batch_invariance_across_gemm_variants(cuda_ok):
         assert moe.moe_read_device_status(ws) == 0
         outs.append(bits(out))
     np.testing.assert_array_equal(outs[0], outs[1][:4095])
+
+
+@pytest.mark.parametrize("name,T,scale", [("fine_grained", 1, 1.0), ("fine_grained", 8, 2.5),
+                                          ("fine_grained", 64, 1.0), ("ling3_tiny", 1, 2.5),
+                                          ("large", 3, 1.0)])
+def test_decode_layer_equals_step_by_step_calls(moe, name, T, scale):
+    """At decode sizes (the swapped GEMM form, the small-batch dispatch and the
+    cluster router) moe_layer_fwd must give the bytes of the step-by-step ABI
+    calls, with a routing scale too, and again on reusing its workspace."""
+    wl = synth.WORKLOADS[name]
+    W = weights(wl)
+    x = synth.tokens(wl, T)
+    wr, bias = synth.router(wl)
+    R = T * wl.k
+    d = moe.dims(T, wl.H, wl.E, wl.k, wl.I)
+    assert moe.moe_expert_ffn_form(d) == 1
+    opts = moe.router_opts(route_scale=scale)
+    xd, wrd, bd = dev_bf16(x), dev(wr), None if bias is None else dev(bias)
+    ws = moe.new_workspace(d)
+    out_layer = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_layer_fwd_ex(xd, wrd, bd, opts, W.packed, d, out_layer, None, None, None, ws)
+    idx = torch.empty((T, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, wl.k), dtype=torch.float32, device="cuda")
+    moe.moe_route_ex(xd, wrd, bd, opts, d, idx, w)
+    counts = torch.empty(wl.E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(wl.E + 1, dtype=torch.int32, device="cuda")
+    ws2 = moe.new_workspace(d)
+    moe.moe_load_stats(idx, d, counts, offsets, ws2)
+    xp = torch.empty((R, wl.H), dtype=torch.bfloat16, device="cuda")
+    ros = torch.empty(R, dtype=torch.int32, device="cuda")
+    sor = torch.empty(R, dtype=torch.int32, device="cuda")
+    moe.moe_permute(xd, idx, offsets, d, xp, ros, sor, ws2)
+    y = torch.empty((R, wl.H), dtype=torch.float32, device="cuda")
+    moe.moe_expert_ffn(xp, offsets, W.packed, d, y, ws2)
+    out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_combine_ex(y, w, ros, scale, d, out)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0 and moe.moe_read_device_status(ws2) == 0
+    np.testing.assert_array_equal(bits(out_layer), bits(out))
+    # twice more through the same workspace
+    for _ in range(2):
+        moe.moe_layer_fwd_ex(xd, wrd, bd, opts, W.packed, d, out_layer, None, None, None, ws)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bits(out_layer), bits(out))

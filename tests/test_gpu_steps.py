@@ -147,3 +147,4 @@ def test_route_kernels_agree_bitwise(moe):
     for T, (idx, w) in zip(Ts[:-1], got[:-1]):
         np.testing.assert_array_equal(idx, big_idx[:T])
         np.testing.assert_array_equal(w.view(np.uint32), big_w[:T].view(np.uint32))
+
