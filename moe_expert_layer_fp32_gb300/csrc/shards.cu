@@ -117,6 +117,11 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// f rounded to bf16 (nearest even), as an FP32 value.
+__device__ __forceinline__ float round_bf16_f32(float f) {
+  return __uint_as_float(f32_to_bf16_bits(f) << 16);
+}
+
 // bf16 bits of s + err, rounded to nearest even, where s = fl(H + L) and err is
 // its exact rounding error (|err| <= half an FP32 ulp of s).
 __device__ __forceinline__ uint32_t round_pair_to_bf16(float s, float err) {
@@ -483,6 +488,231 @@ __global__ void __launch_bounds__(kShardWarps * 32, 4) combine_sharded_kernel(
   }
 }
 
+// The layer's sharded combine, when no partials are asked for: one CTA per token
+// and column block, four columns per thread per step, the k rows read with
+// 16-byte loads as in the plain combine.  The per-token schedule (positions in
+// rank order, a mask that restarts the chain at each run's first position, the
+// run ends) is built by one warp in parallel (lane = slot), sits in registers
+// before the column loop, and the run-end test is a branch that is the same for
+// the whole CTA.
+//
+// The chains here leave out the signed-zero adds of the plan: they change a
+// run's value only while it is exactly zero (once a chain is non-zero its later
+// values do not depend on the sign of an earlier zero), and a zero leaf sends its
+// column to the literal routine below.  Per column: when every leaf is non-zero,
+// below 2^124, and within one window of 16 - ceil(log2 GM) binades, their plain
+// FP32 sum is exact in any order and equals the FP64 tree's value, rounded once
+// to bf16; any other column (a zero, inf or NaN leaf, a wider spread) is marked
+// and, after the streaming loop, computed by literal_element, the definition itself.
+template <int GM, int KP, bool SHARED>
+__global__ void __launch_bounds__(128) combine_sharded_fast_kernel(
+    const float* __restrict__ y, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ row_of_slot,
+    const int32_t* __restrict__ owner, int G, int T, int H, int E, int k, float scale,
+    const float* __restrict__ shared, uint16_t* __restrict__ out) {
+  constexpr float kScale = (float)(1u << (16 - ceil_log2(GM)));
+  __shared__ int s_row[kMaxK];
+  __shared__ int s_own[kMaxK];
+  __shared__ float s_w[kMaxK];
+  __shared__ TokenPlan s_plan;
+  __shared__ uint32_t s_redo[16384 / 32];  // columns for the literal routine (H <= 16384)
+  const int t = blockIdx.x;
+  const long long R = (long long)T * k;
+  for (int i = threadIdx.x; i < H / gridDim.y / 32; i += blockDim.x) s_redo[i] = 0u;
+  if (threadIdx.x < 32) {
+    // the schedule, warp-parallel: lane j is slot j.  Positions are the owned slots
+    // sorted by rank, slot order within a rank (build_plan's order); the run of a
+    // rank starts at its first position and ends at its last.
+    const int j = threadIdx.x;
+    int r = -1, o = -1;
+    float wj = 0.0f;
+    if (j < k) {
+      r = row_of_slot[(size_t)t * k + j];
+      const int e = topk_idx[(size_t)t * k + j];
+      o = (e >= 0 && e < E) ? owner[e] : -1;
+      r = (r >= 0 && r < R) ? r : -1;
+      o = (o >= 0 && o < G) ? o : -1;  // -1: no rank owns the slot
+      wj = __fmul_rn(scale, topk_w[(size_t)t * k + j]);
+      s_row[j] = r;
+      s_own[j] = o;
+      s_w[j] = wj;
+    }
+    const bool pos = j < k && r >= 0 && o >= 0;  // the slot joins its rank's run
+    int before = 0, same_before = 0, same_after = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxK; ++i) {
+      const int oi = __shfl_sync(0xFFFFFFFFu, pos ? o : -1, i);
+      if (i < k && oi >= 0) {
+        before += (oi < o) || (oi == o && i < j);
+        same_before += oi == o && i < j;
+        same_after += oi == o && i > j;
+      }
+    }
+    const unsigned first = __reduce_or_sync(0xFFFFFFFFu, pos && same_before == 0 ? 1u << before : 0u);
+    const unsigned last = __reduce_or_sync(0xFFFFFFFFu, pos && same_after == 0 ? 1u << before : 0u);
+    const unsigned runs = __reduce_or_sync(0xFFFFFFFFu, pos ? 1u << o : 0u);
+    const unsigned npos = __popc(__ballot_sync(0xFFFFFFFFu, pos));
+    const bool bad_w = __any_sync(0xFFFFFFFFu, j < k && r >= 0 && !isfinite(wj));
+    if (pos) {
+      s_plan.row[before] = r;
+      s_plan.rank[before] = o;
+      s_plan.w[before] = wj;
+    }
+    if (j == 0) {
+      s_plan.n_pos = (int)npos;
+      s_plan.literal = bad_w ? 1 : 0;
+      s_plan.first = first;
+      s_plan.last = last;
+      s_plan.has_run = runs;
+    }
+  }
+  __syncthreads();
+  const int cols = H / gridDim.y;
+  const int cb = blockIdx.y * cols;
+  const float* sh = SHARED ? shared : nullptr;
+  uint16_t* orow = out + (size_t)t * H;
+  if (s_plan.literal) {
+    for (int c = cb + threadIdx.x; c < cb + cols; c += blockDim.x)
+      orow[c] = (uint16_t)literal_element(y, s_row, s_own, s_w, k, G, sh, T, H, t, c, nullptr);
+    return;
+  }
+  const int n_pos = s_plan.n_pos;
+  const uint32_t last = s_plan.last;
+  const uint32_t no_run = ((1u << G) - 1u) & ~s_plan.has_run;
+  int prow[KP], prank[KP];
+  float pw[KP];
+  uint32_t keep[KP];  // 0: the position starts its rank's run (the chain restarts at +0)
+#pragma unroll
+  for (int p = 0; p < KP; ++p) {
+    prow[p] = (p < n_pos) ? s_plan.row[p] : 0;
+    prank[p] = (p < n_pos) ? s_plan.rank[p] : 0;
+    pw[p] = (p < n_pos) ? s_plan.w[p] : 0.0f;
+    keep[p] = ((s_plan.first >> p) & 1u) ? 0u : 0xFFFFFFFFu;
+  }
+  // a rank without a slot contributes +0 (no shard) or bf16(+0 + its shard)
+  const float s0 = no_run != 0u ? 0.0f : -0.0f;
+  int any_redo = 0;
+  // the rows of the next step are in flight while this one is computed
+  float4 vn[KP];
+  const int cstart = cb + threadIdx.x * 4, cend = cb + cols, cstep = blockDim.x * 4;
+#pragma unroll
+  for (int p = 0; p < KP; ++p)
+    if (p < n_pos && cstart < cend)
+      vn[p] = __ldg(reinterpret_cast<const float4*>(y + (size_t)prow[p] * H + cstart));
+  for (int c = cstart; c < cend; c += cstep) {
+    float4 v[KP];
+#pragma unroll
+    for (int p = 0; p < KP; ++p) v[p] = vn[p];
+    if (c + cstep < cend) {
+#pragma unroll
+      for (int p = 0; p < KP; ++p)
+        if (p < n_pos) vn[p] = __ldg(reinterpret_cast<const float4*>(y + (size_t)prow[p] * H + c + cstep));
+    }
+    float4 q[SHARED ? KP : 1];
+    if constexpr (SHARED) {
+#pragma unroll
+      for (int p = 0; p < KP; ++p)
+        if (p < n_pos && ((last >> p) & 1u))
+          q[p] = __ldg(reinterpret_cast<const float4*>(shared + ((size_t)prank[p] * T + t) * H + c));
+    }
+    float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float sum[4] = {s0, s0, s0, s0};
+    float mx[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float mn[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mn[i] = __int_as_float(0x7F800000);
+#pragma unroll
+    for (int p = 0; p < KP; ++p) {
+      if (p < n_pos) {
+        const float vv[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          a[i] = fmaf(pw[p], vv[i], __uint_as_float(__float_as_uint(a[i]) & keep[p]));
+        if ((last >> p) & 1u) {
+          float qq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if constexpr (SHARED) {
+            qq[0] = q[p].x;
+            qq[1] = q[p].y;
+            qq[2] = q[p].z;
+            qq[3] = q[p].w;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float lf = round_bf16_f32(SHARED ? __fadd_rn(a[i], qq[i]) : a[i]);
+            sum[i] = __fadd_rn(sum[i], lf);
+            mx[i] = fmaxf(mx[i], fabsf(lf));
+            mn[i] = fminf(mn[i], fabsf(lf));
+          }
+        }
+      }
+    }
+    if constexpr (SHARED) {
+#pragma unroll
+      for (int g = 0; g < GM; ++g) {
+        if (g < G && ((no_run >> g) & 1u)) {
+          const float4 qg = __ldg(reinterpret_cast<const float4*>(shared + ((size_t)g * T + t) * H + c));
+          const float qv[4] = {qg.x, qg.y, qg.z, qg.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float lf = round_bf16_f32(__fadd_rn(0.0f, qv[i]));
+            sum[i] = __fadd_rn(sum[i], lf);
+            mx[i] = fmaxf(mx[i], fabsf(lf));
+            mn[i] = fminf(mn[i], fabsf(lf));
+          }
+        }
+      }
+    }
+    uint32_t o[4];
+    uint32_t bad = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const bool ok = mx[i] < __int_as_float(0x7D800000) && mn[i] > 0.0f &&
+                      mx[i] < mn[i] * kScale && sum[i] == sum[i];
+      o[i] = f32_to_bf16_bits(sum[i]);
+      if (!ok) bad |= 1u << i;
+    }
+    *reinterpret_cast<uint2*>(orow + c) = make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
+    if (bad != 0u) {  // redone below by this thread, outside the streaming loop
+      atomicOr(&s_redo[(c - cb) >> 5], bad << ((c - cb) & 31));
+      any_redo = 1;
+    }
+  }
+  // the rare columns one window could not take: their leaves again (the chains from
+  // L2), then the exact two-window sum of exact_pair_sum, and where that cannot
+  // decide either (a zero leaf, whose sign the chains above do not settle, a spread
+  // beyond two windows, inf, NaN) the definition itself
+  if (__syncthreads_or(any_redo)) {
+    constexpr int kW = 16 - ceil_log2(GM);
+    for (int c = cstart; c < cend; c += cstep) {
+      const uint32_t bad = (s_redo[(c - cb) >> 5] >> ((c - cb) & 31)) & 0xFu;
+      for (int i = 0; i < 4; ++i) {
+        if (!((bad >> i) & 1u)) continue;
+        const int col = c + i;
+        uint32_t words[KP];
+        bool zero_leaf = false;
+        float a = 0.0f;
+#pragma unroll
+        for (int p = 0; p < KP; ++p) {
+          words[p] = 0u;
+          if (p < n_pos) {
+            a = fmaf(pw[p], __ldg(y + (size_t)prow[p] * H + col),
+                     __uint_as_float(__float_as_uint(a) & keep[p]));
+            if ((last >> p) & 1u) {
+              const uint32_t lb = f32_to_bf16_bits(a);
+              words[p] = lb | (lb << 16);
+              zero_leaf |= (lb & 0x7FFFu) == 0u;
+            }
+          }
+        }
+        uint32_t o = 0u;
+        if (zero_leaf || (exact_pair_sum<KP, kW>(words, last, no_run == 0u, o) & 1u))
+          o = literal_element(y, s_row, s_own, s_w, k, G, sh, T, H, t, col, nullptr);
+        orow[col] = (uint16_t)(o & 0xFFFFu);
+      }
+    }
+  }
+}
+
 // The FP64 tree over element n of the G rows, from memory.
 __device__ __forceinline__ uint32_t tree_element_fp64(const uint16_t* __restrict__ partials, int G,
                                                    long long N, long long n) {
@@ -559,6 +789,17 @@ cudaError_t launch_combine_gm(const float* y, const float* topk_w, const int32_t
                               const int32_t* row_of_slot, const int32_t* owner, int G, int T, int H,
                               int E, int k, float scale, const float* shared, uint16_t* partials,
                               uint16_t* out, cudaStream_t s) {
+  if (partials == nullptr && shared == nullptr) {
+    // split each token's columns over up to H / 512 CTAs while the grid stays within
+    // four CTAs per SM (as the plain combine does)
+    int split = 1;
+    while (split * 2 <= H / 512 && H % (split * 2 * 512) == 0 &&
+           (long long)T * split * 2 <= 4LL * device_sm_count())
+      split *= 2;
+    combine_sharded_fast_kernel<GM, KP, false><<<dim3(T, split), 128, 0, s>>>(
+        y, topk_w, topk_idx, row_of_slot, owner, G, T, H, E, k, scale, nullptr, out);
+    return cudaGetLastError();
+  }
   const int grid = (T + kShardWarps - 1) / kShardWarps;
   if (shared != nullptr)
     combine_sharded_kernel<GM, KP, true><<<grid, kShardWarps * 32, 0, s>>>(

@@ -159,6 +159,10 @@ def test_combine_sharded_golden_cases(moe):
         assert bits(out)[:, 0].tolist() == [v[0] for v in c["expected_out_bf16_bits"]], c["name"]
         np.testing.assert_array_equal(bits(parts)[:, :, :1],
                                       np.array(c["expected_partials_bf16_bits"]))
+        out2 = torch.empty_like(out)  # the layer's form (no partials written)
+        moe.moe_combine_sharded(dev(y), dev(w), dev(idx), dev(ros), dev(owner), G, 1.0,
+                                None if sh is None else dev(sh), d, out2)
+        assert bits(out2)[:, 0].tolist() == [v[0] for v in c["expected_out_bf16_bits"]], c["name"]
 
 
 def test_sharded_layer_on_gpu_expert_outputs(moe):
@@ -204,7 +208,7 @@ def test_combine_sharded_signed_zeros_and_fallback(moe, G):
     """Inputs built so that the chain order shows in the sign of zero (products
     that underflow to -0, weights of both signs, exact zeros), and shard outputs
     spread over 40 binades so that part of the tree falls back to FP64.  Partials
-    and outputs bit-exact."""
+    and outputs bit-exact, with and without the partials output (two kernels)."""
     T, H, E, k = 300, 128, 16, 8
     rng = np.random.default_rng(G)
     idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
@@ -229,3 +233,7 @@ def test_combine_sharded_signed_zeros_and_fallback(moe, G):
                                                 want_partials=True)
         np.testing.assert_array_equal(bits(parts), ref_parts)
         np.testing.assert_array_equal(bits(out), ref)
+        out2 = torch.empty_like(out)  # the layer's form (no partials written)
+        moe.moe_combine_sharded(dev(y), dev(w), dev(idx), dev(ros), dev(owner), G, 1.0,
+                                None if shared is None else dev(shared), d, out2)
+        np.testing.assert_array_equal(bits(out2), ref)
