@@ -35,8 +35,24 @@ def headers():
                   [os.path.join(ROOT, "include", "moe.h")])
 
 
+def built_for_this_machine(path: str) -> bool:
+    """The library's ELF machine field matches this host (x86_64 or aarch64): a
+    library copied from a machine of the other architecture is rebuilt."""
+    import platform
+    want = {"x86_64": 0x3E, "amd64": 0x3E, "aarch64": 0xB7, "arm64": 0xB7}.get(
+        platform.machine().lower())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF":
+        return False
+    return want is None or int.from_bytes(head[18:20], "little") == want
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not built_for_this_machine(LIB):
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(p) <= t for p in sources() + headers() + [__file__])
@@ -44,6 +60,7 @@ def up_to_date() -> bool:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
+        print(f"{LIB}: up to date (built here, newer than every source)", file=sys.stderr)
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
