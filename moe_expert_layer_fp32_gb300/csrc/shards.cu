@@ -516,23 +516,32 @@ __global__ void __launch_bounds__(128) combine_sharded_fast_kernel(
   __shared__ float s_w[kMaxK];
   __shared__ TokenPlan s_plan;
   __shared__ uint32_t s_redo[16384 / 32];  // columns for the literal routine (H <= 16384)
+  __shared__ int s_owner[kMaxE];            // the owner table, read with the slots
   const int t = blockIdx.x;
   const long long R = (long long)T * k;
   for (int i = threadIdx.x; i < H / gridDim.y / 32; i += blockDim.x) s_redo[i] = 0u;
+  // the slots' loads and the owner table's go out together (one round trip)
+  int r = -1, e = -1;
+  float wraw = 0.0f;
+  if (threadIdx.x < k) {
+    r = row_of_slot[(size_t)t * k + threadIdx.x];
+    e = topk_idx[(size_t)t * k + threadIdx.x];
+    wraw = topk_w[(size_t)t * k + threadIdx.x];
+  }
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_owner[i] = __ldg(owner + i);
+  __syncthreads();
   if (threadIdx.x < 32) {
     // the schedule, warp-parallel: lane j is slot j.  Positions are the owned slots
     // sorted by rank, slot order within a rank (build_plan's order); the run of a
     // rank starts at its first position and ends at its last.
     const int j = threadIdx.x;
-    int r = -1, o = -1;
+    int o = -1;
     float wj = 0.0f;
     if (j < k) {
-      r = row_of_slot[(size_t)t * k + j];
-      const int e = topk_idx[(size_t)t * k + j];
-      o = (e >= 0 && e < E) ? owner[e] : -1;
+      o = (e >= 0 && e < E) ? s_owner[e] : -1;
       r = (r >= 0 && r < R) ? r : -1;
       o = (o >= 0 && o < G) ? o : -1;  // -1: no rank owns the slot
-      wj = __fmul_rn(scale, topk_w[(size_t)t * k + j]);
+      wj = __fmul_rn(scale, wraw);
       s_row[j] = r;
       s_own[j] = o;
       s_w[j] = wj;
