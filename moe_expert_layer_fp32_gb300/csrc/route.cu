@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(NTHR, 4) route_kernel(const uint16_t* __restri
     }
     __syncthreads();
     const float* wsb = ws + buf * HK * EP;
-#pragma unroll 8
+#pragma unroll (HK > 16 ? 8 : HK)
     for (int hh = 0; hh < HK; ++hh) {
       float2 xp[TT];
       load_x8(xsc + hh * XLD + warp * TT, 4, xp);
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(NTHR, 4) route_tile_kernel(const uint16_t* __r
     }
     __syncthreads();
     const float* wsb = ws + buf * HK * EP;
-#pragma unroll 4
+#pragma unroll
     for (int hh = 0; hh < HK; ++hh) {
       float2 xp[8];
       load_x8(xsc + hh * XL + tb, 4 * LT, xp);

@@ -1,6 +1,6 @@
 """Edge cases and device-side checks of the CUDA path: empty batches, a single
-token, ragged tails, degenerate expert counts (E = 1, k = E), the largest E and
-k, caller-supplied routing, and malformed indices/offsets that the kernels must
+token, ragged tails, degenerate expert counts (E = 1, k = E), the largest E, k
+and H, caller-supplied routing, and malformed indices/offsets that the kernels must
 flag instead of touching memory out of range."""
 import numpy as np
 import pytest
@@ -86,6 +86,16 @@ def test_degenerate_shapes_in_swapped_form(moe, name, T, E, k):
     GEMMs with the weight rows on the MMA's M side."""
     wl = synth.Workload(name, T=T, H=256, E=E, k=k, I=128, w_std=0.05, wr_std=0.5)
     assert moe.moe_expert_ffn_form(moe.dims(T, wl.H, E, k, wl.I)) == 1
+    layer_vs_oracle(moe, wl)
+
+
+@pytest.mark.parametrize("T", [2, 300])
+def test_largest_hidden_size(moe, T):
+    """H = 16384, the library's largest hidden size: 256 k-blocks per GEMM tile and
+    the router's longest FMA chains, in the swapped form (T = 2) and the tile form
+    (T = 300)."""
+    wl = synth.Workload("wide_h", T=T, H=16384, E=4, k=2, I=256, w_std=0.01, wr_std=0.01)
+    assert moe.moe_expert_ffn_form(moe.dims(T, wl.H, wl.E, wl.k, wl.I)) == (1 if T == 2 else 0)
     layer_vs_oracle(moe, wl)
 
 
