@@ -17,6 +17,7 @@
 // idle; every element's chain is the same either way.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -33,6 +34,10 @@ __global__ void __launch_bounds__(128, SPLIT ? 5 : 0) combine_kernel(const float
   __shared__ float s_w[kMaxK];
   const int t = blockIdx.x;
   const long long R = (long long)T * k;
+  // a programmatic dependent of the down GEMM: y, the weights and the rows are
+  // read (and out written) only after it has finished
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
   if (threadIdx.x < k) {
     const int r = row_of_slot[(size_t)t * k + threadIdx.x];
     s_row[threadIdx.x] = (r >= 0 && r < R) ? r : -1;
@@ -86,12 +91,10 @@ cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* r
          (long long)T * split * 2 <= 4LL * device_sm_count())
     split *= 2;
   if (split > 1)
-    combine_kernel<true><<<dim3(T, split), 128, 0, s>>>(y, topk_w, row_of_slot, T, H, k, scale,
-                                                        static_cast<uint16_t*>(out));
-  else
-    combine_kernel<false><<<T, 128, 0, s>>>(y, topk_w, row_of_slot, T, H, k, scale,
-                                            static_cast<uint16_t*>(out));
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<true>, dim3(T, split), dim3(128), 0, s, y, topk_w,
+                      row_of_slot, T, H, k, scale, static_cast<uint16_t*>(out));
+  return launch_pdl(combine_kernel<false>, dim3(T), dim3(128), 0, s, y, topk_w, row_of_slot, T, H,
+                    k, scale, static_cast<uint16_t*>(out));
 }
 
 }  // namespace moe

@@ -16,6 +16,7 @@
 // integer function of topk_idx alone: bit-identical on every run and for every T.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -195,6 +196,10 @@ __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __res
     const int cc = u * 32 + lane;
     if (t < T && cc < nv) v0[u] = __ldg(src + cc);
   }
+  // a programmatic dependent of the router: the routing is read, and every
+  // output written, after it has finished (x was final before the router began)
+  pdl_wait();
+  if (tid == 0) pdl_launch_dependents();
   // every CTA ranks the whole (single) block; each then copies its own 8 tokens
   build_masks(topk_idx, T, k, E, 0, masks, sidx, blockIdx.x == 0 ? status : nullptr);
   int c = 0;
@@ -381,10 +386,9 @@ cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, 
                                   int32_t* slot_of_row, void* x_perm, int32_t* status,
                                   cudaStream_t s) {
   const int nb = T > 0 ? (T + 7) / 8 : 1;
-  dispatch_small_kernel<<<nb, PB, mask_smem_bytes(E, k), s>>>(
-      topk_idx, T, k, E, static_cast<const uint16_t*>(x), H, counts, offsets, row_of_slot,
-      slot_of_row, static_cast<uint16_t*>(x_perm), status);
-  return cudaGetLastError();
+  return launch_pdl(dispatch_small_kernel, dim3(nb), dim3(PB), mask_smem_bytes(E, k), s, topk_idx,
+                    T, k, E, static_cast<const uint16_t*>(x), H, counts, offsets, row_of_slot,
+                    slot_of_row, static_cast<uint16_t*>(x_perm), status);
 }
 
 namespace {

@@ -48,6 +48,7 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -56,26 +57,33 @@ constexpr int SK = 64;                       // k-block: one 128-byte swizzle ro
 constexpr int SUK = 16;                      // MMA K
 constexpr int WROWS = 256;                   // rows of one packed weight box
 constexpr int HALF = 128;                    // MMA M
-constexpr int TT = 64;                       // token rows per unit at most (MMA N <= 64)
-constexpr int X_BYTES = TT * SK * 2;         // 8 KB (N = 64)
+constexpr int kTT = 64;                      // token rows per unit at most (MMA N <= 64)
 
 // HV selects the unit: 2 = a whole packed box (two M = 128 MMAs per K step; gate
 // and up meet in one CTA), 1 = one 128-row half of a box (down only), 4 = 64 gate
 // rows + the matching 64 up rows of a box in one M = 128 operand (gate/up only).
-template <int HV>
+// TT: token rows per unit at most: 64, or 16 when the whole batch has at most 16
+// rows (T <= 2 for k = 8).  The down GEMM is a programmatic dependent launch of
+// the gate/up GEMM: its CTAs start on SMs with room while the gate/up GEMM runs
+// and stream their first weight stages before they wait for h.  The TT = 16
+// quarter and half units hold five stages of 16 KB + a 2 KB token box (at most
+// ~110 KB), so a gate/up CTA and a down CTA fit on one SM together.
+template <int HV, int TT = kTT>
 struct SwapCfg {
   static constexpr int UROWS = HV == 2 ? 2 * HALF : HALF;  // weight rows per unit
   static constexpr int NMMA = HV == 2 ? 2 : 1;             // M = 128 MMAs per K step
-  static constexpr int STAGES = HV == 2 ? 5 : 8;
+  static constexpr int X_BYTES = TT * SK * 2;              // token box (N = TT)
+  static constexpr int STAGES = (HV == 2 || TT == 16) ? 5 : 8;
   static constexpr int W_BYTES = UROWS * SK * 2;           // 32 or 16 KB
-  static constexpr int ACC_COLS = NMMA * TT;               // one accumulator buffer
+  static constexpr int HOFF = TT < 32 ? 32 : TT;           // TMEM columns per half (32-aligned)
+  static constexpr int ACC_COLS = NMMA * HOFF;             // one accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS;           // double-buffered
   static constexpr int NBAR = 2 * STAGES + 2 + 2 + 1;
-  // HV = 4: up values of 64 weight rows x 64 token rows, passed to the gate warps
+  // HV = 4: up values of 64 weight rows x TT token rows, passed to the gate warps
   static constexpr int XCH_BYTES = HV == 4 ? 64 * (TT + 1) * 4 : 0;
   static constexpr int SMEM_BYTES = 1024 + STAGES * (W_BYTES + X_BYTES) + XCH_BYTES + NBAR * 8 +
                                     16 + 3 * (kMaxE + 1) * 4;
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(SMEM_BYTES <= (TT == 16 && HV != 2 ? 110 : 227) * 1024, "shared memory");
 };
 
 // Weight boxes (UROWS rows; 64 for HV = 4) and token boxes of 16, 32 and 64 rows;
@@ -92,7 +100,7 @@ struct SwapWork {
   int w_load_row;  // box row of k-block 0 in the packed weights
 };
 
-template <int HV>
+template <int HV, int TT>
 __device__ __forceinline__ SwapWork swap_decode(int u, const int* s_prefix, const int* s_off,
                                                 const int* s_tt, int E, int NTW, int KB,
                                                 int a_local) {
@@ -111,7 +119,7 @@ __device__ __forceinline__ SwapWork swap_decode(int u, const int* s_prefix, cons
   const int ti = local - w.wt * tt;
   w.row0 = s_off[lo] + ti * TT;
   w.rows = min(TT, s_off[lo + 1] - w.row0);
-  w.nb = w.rows <= 16 ? 16 : (w.rows <= 32 ? 32 : 64);
+  w.nb = (TT == 16 || w.rows <= 16) ? 16 : (w.rows <= 32 ? 32 : 64);
   w.x_load_row = w.row0 - (a_local ? s_off[lo] : 0);
   // box row of (expert, box, k-block 0), plus the unit's rows within the box:
   // HV = 1 its 128-row half, HV = 4 its 64 gate rows (its up rows are 128 further)
@@ -136,15 +144,16 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
-template <bool SWIGLU, int HV>
+template <bool SWIGLU, int HV, int TT, bool DEP>
 __global__ void __launch_bounds__(192, 1)
     grouped_gemm_swap_kernel(const __grid_constant__ SwapMaps maps,
                              const int32_t* __restrict__ offsets, int E, int R, int n_per_expert,
                              int K, void* __restrict__ out, int out_ld, int32_t* status,
                              long long spin_limit, int a_local) {
-  using C = SwapCfg<HV>;
+  using C = SwapCfg<HV, TT>;
   static_assert(SWIGLU ? HV != 1 : HV != 4, "gate and up rows of a unit must meet in one CTA");
   constexpr int STAGES = C::STAGES, W_BYTES = C::W_BYTES, ACC_COLS = C::ACC_COLS;
+  constexpr int X_BYTES = C::X_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -167,6 +176,36 @@ __global__ void __launch_bounds__(192, 1)
   const int NTW = n_per_expert / C::UROWS;  // units per expert (and token tile)
   const int KB = K / SK;
 
+  // prologue that touches no memory the previous kernel writes: barriers, tensor
+  // maps (kernel parameters), tensor memory
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&maps.w);
+    prefetch_tensormap(&maps.x16);
+    prefetch_tensormap(&maps.x32);
+    prefetch_tensormap(&maps.x64);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  // The gate/up GEMM waits here for the kernel that wrote the offsets and the
+  // token rows, then lets the down GEMM start.  The down GEMM (DEP) reads the
+  // offsets at once (their writer finished before the gate/up GEMM passed this
+  // point) and waits only before its first load of h, the gate/up output.
+  if constexpr (!DEP) {
+    pdl_wait();
+    if (threadIdx.x == 0) pdl_launch_dependents();
+  }
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = __ldg(offsets + e);
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -187,25 +226,7 @@ __global__ void __launch_bounds__(192, 1)
       p = 0;
     }
     s_prefix[E] = p;
-    *abort_flag = 0;
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
-    }
-    mbar_init(mma_done, 1);
-    fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&maps.w);
-    prefetch_tensormap(&maps.x16);
-    prefetch_tensormap(&maps.x32);
-    prefetch_tensormap(&maps.x64);
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -217,14 +238,33 @@ __global__ void __launch_bounds__(192, 1)
       // ------------------------------------------------------------ producer
       int it = 0;
       bool aborted = false;
-      for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
-        const SwapWork w = swap_decode<HV>(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
+      bool first = true;
+      for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x, first = false) {
+        const SwapWork w = swap_decode<HV, TT>(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
         const CUtensorMap* xm = w.nb == 16 ? &maps.x16 : (w.nb == 32 ? &maps.x32 : &maps.x64);
         const uint32_t bytes = W_BYTES + w.nb * SK * 2;
+        // DEP (a dependent launch): the first unit's first stages get their weight
+        // boxes now and their token boxes (rows of the previous grid's output) only
+        // after griddepcontrol.wait, i.e. once that grid has finished and its
+        // writes are visible
+        const int ndefer = (DEP && first) ? min(STAGES, KB) : 0;
+        const int it0 = it;
+        // (also on an abort: every armed stage then still receives its bytes, so
+        // the drain below ends)
+        auto load_deferred = [&](int n) {
+          pdl_wait();
+          pdl_launch_dependents();  // the combine may start; it waits for this grid
+          for (int j = 0; j < n; ++j) {
+            const int sj = (it0 + j) % STAGES;
+            tma_load_2d(xm, sX + sj * X_BYTES, &full[sj], j * SK, w.x_load_row);
+          }
+        };
         for (int kb = 0; kb < KB; ++kb, ++it) {
+          if (kb == ndefer && ndefer > 0) load_deferred(ndefer);
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, status, spin_limit)) {
+            if (kb < ndefer) load_deferred(kb);
             aborted = true;
             break;
           }
@@ -233,8 +273,9 @@ __global__ void __launch_bounds__(192, 1)
           if constexpr (HV == 4)  // the matching up rows, into operand rows 64..127
             tma_load_2d(&maps.w, sW + s * W_BYTES + 64 * 128, &full[s], 0,
                         w.w_load_row + HALF + kb * WROWS);
-          tma_load_2d(xm, sX + s * X_BYTES, &full[s], kb * SK, w.x_load_row);
+          if (kb >= ndefer) tma_load_2d(xm, sX + s * X_BYTES, &full[s], kb * SK, w.x_load_row);
         }
+        if (ndefer > 0 && ndefer == KB && !aborted) load_deferred(ndefer);
       }
       if (aborted) {
         for (int i = (it > STAGES ? it - STAGES : 0); i < it; ++i)
@@ -246,13 +287,13 @@ __global__ void __launch_bounds__(192, 1)
       // ---------------------------------------------------------- MMA issuer
       int it = 0, tcount = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
-        const SwapWork w = swap_decode<HV>(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
+        const SwapWork w = swap_decode<HV, TT>(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
         const uint32_t idesc = idesc_bf16_f32(HALF, w.nb);
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (!mbar_wait_bounded(&tempty[acc], aph ^ 1, abort_flag, status, spin_limit)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + acc * ACC_COLS;  // half 0; half 1 at + TT
+        const uint32_t d0 = tmem_base + acc * ACC_COLS;  // half 0; half 1 at + HOFF
         bool aborted = false;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
@@ -270,7 +311,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             mma_bf16(d0, sdesc_k_major_sw128(w_addr + kk * SUK * 2), xd, idesc, accum);
             if constexpr (HV == 2)
-              mma_bf16(d0 + TT, sdesc_k_major_sw128(w_addr + HALF * 128 + kk * SUK * 2), xd,
+              mma_bf16(d0 + C::HOFF, sdesc_k_major_sw128(w_addr + HALF * 128 + kk * SUK * 2), xd,
                        idesc, accum);
           }
           mma_commit(&empty[s]);
@@ -287,7 +328,7 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;
     int tcount = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
-      const SwapWork w = swap_decode<HV>(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
+      const SwapWork w = swap_decode<HV, TT>(u, s_prefix, s_off, s_tt, E, NTW, KB, a_local);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       int ok = 1;
@@ -335,7 +376,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int j0 = 0; j0 < w.nb; j0 += 16) {
           uint32_t g[16], uu[16];
           tmem_ld_32x32b_x16(taddr + j0, g);
-          tmem_ld_32x32b_x16(taddr + TT + j0, uu);
+          tmem_ld_32x32b_x16(taddr + C::HOFF + j0, uu);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -354,7 +395,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int c = 0; c < C::NMMA; ++c) {
           for (int j0 = 0; j0 < w.nb; j0 += 16) {
             uint32_t v[16];
-            tmem_ld_32x32b_x16(taddr + c * TT + j0, v);
+            tmem_ld_32x32b_x16(taddr + c * C::HOFF + j0, v);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -377,22 +418,25 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <bool SWIGLU, int HV>
-cudaError_t launch_swap(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets, int E,
-                        int R, int n_per_expert, int K, void* out, int out_ld, int32_t* status,
-                        long long spin_limit, cudaStream_t s, int a_local) {
+template <bool SWIGLU, int HV, int TT>
+cudaError_t launch_swap_tt(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets,
+                           int E, int R, int n_per_expert, int K, void* out, int out_ld,
+                           int32_t* status, long long spin_limit, cudaStream_t s, int a_local) {
   SwapMaps m;
-  using C = SwapCfg<HV>;
+  using C = SwapCfg<HV, TT>;
+  // both GEMMs are programmatic dependent launches; the down GEMM (DEP) streams
+  // weights before it waits
+  constexpr bool DEP = !SWIGLU;
+  auto kern = grouped_gemm_swap_kernel<SWIGLU, HV, TT, DEP>;
   if (!b.encode(&m.w, HV == 4 ? 64 : C::UROWS) || !a.encode(&m.x16, 16) || !a.encode(&m.x32, 32) ||
-      !a.encode(&m.x64, TT))
+      !a.encode(&m.x64, 64))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !attr_set[dev]) {
-    err = cudaFuncSetAttribute(grouped_gemm_swap_kernel<SWIGLU, HV>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     if (dev < 64) attr_set[dev] = true;
   }
@@ -401,9 +445,30 @@ cudaError_t launch_swap(const GemmOperand& a, const GemmOperand& b, const int32_
   const long long units =
       (long long)(n_per_expert / C::UROWS) * (std::min<long long>(E, R) + R / TT);
   const int grid = (int)std::max<long long>(1, std::min<long long>(device_sm_count(), units));
-  grouped_gemm_swap_kernel<SWIGLU, HV><<<grid, 192, C::SMEM_BYTES, s>>>(
-      m, offsets, E, R, n_per_expert, K, out, out_ld, status, spin_limit, a_local);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  pdl_attr(attr[0]);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, m, offsets, E, R, n_per_expert, K, out, out_ld, status,
+                            spin_limit, a_local);
+}
+
+// TT = 16 when the whole batch has at most 16 rows (every expert then has at most
+// 16): the same N = 16 MMAs per row as with TT = 64.
+template <bool SWIGLU, int HV>
+cudaError_t launch_swap(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets, int E,
+                        int R, int n_per_expert, int K, void* out, int out_ld, int32_t* status,
+                        long long spin_limit, cudaStream_t s, int a_local) {
+  if (R <= 16)
+    return launch_swap_tt<SWIGLU, HV, 16>(a, b, offsets, E, R, n_per_expert, K, out, out_ld,
+                                          status, spin_limit, s, a_local);
+  return launch_swap_tt<SWIGLU, HV, kTT>(a, b, offsets, E, R, n_per_expert, K, out, out_ld, status,
+                                         spin_limit, s, a_local);
 }
 
 }  // namespace

@@ -37,6 +37,7 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -591,6 +592,10 @@ __global__ void __launch_bounds__(ClusterCfg<EP, TSV, CC>::NTH)
   const int t0 = (blockIdx.x / CC) * TSV;   // the cluster's first token
   const int nchunks = (H + HC - 1) / HC;  // the last one may hold fewer rows (H % 128 == 0)
   const int ecols = max(0, min(EC, E - e0));  // valid experts of this CTA
+  // a programmatic dependent launch: x (often the previous kernel's output), the
+  // router weights and the outputs are touched only after that kernel finished
+  pdl_wait();
+  if (tid == 0) pdl_launch_dependents();
 
   if (ecols < EC) {  // experts past E read zeros for the whole kernel
     for (int i = tid; i < CNST * HC * EC; i += NTH)
@@ -698,25 +703,28 @@ cudaError_t launch_cluster(const void* x, const float* wr, const float* bias, in
       return launch_cluster<EP, TSV, KIND, kCC>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CC;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  pdl_attr(attr[1]);
   cfg.gridDim = dim3(CC * ((T + TSV - 1) / TSV));
   cfg.blockDim = dim3(C::NTH);
   cfg.dynamicSmemBytes = C::bytes;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (known == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::bytes);
     if (e != cudaSuccess) return e;
     if constexpr (CC > 8) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       int clusters = 0;
-      if (e != cudaSuccess || cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess ||
-          clusters < 1) {
+      cfg.numAttrs = 1;  // the query takes the cluster shape alone
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+      cfg.numAttrs = 2;
+      if (e != cudaSuccess || clusters < 1) {
         (void)cudaGetLastError();
         if (dv < 64) ok[dv] = -1;
         return launch_cluster<EP, TSV, KIND, kCC>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
