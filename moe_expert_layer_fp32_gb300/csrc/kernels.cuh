@@ -87,6 +87,12 @@ struct GemmOperand {
   bool encode(CUtensorMap* map, uint32_t box_rows) const;
 };
 
+// A row-major 2D tensor [rows, cols] of FP32 (fp32) or BF16 elements, boxes of
+// box_cols x box_rows without swizzle, zeros outside; false if the driver
+// refuses it (base not 16-byte aligned, row stride not a multiple of 16 bytes).
+bool encode_rowmajor_2d(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows, bool fp32,
+                        uint32_t box_cols, uint32_t box_rows);
+
 // grouped GEMM-1 with the SwiGLU epilogue: a = x_perm [R, H], b = packed W1
 // [E*2I, H] -> h [R, I] bf16.  a_local: every group reads rows of `a` from 0
 // (one token matrix for all groups, e.g. the column shards of a shared expert).

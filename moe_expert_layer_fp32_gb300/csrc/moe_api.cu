@@ -178,6 +178,22 @@ bool GemmOperand::encode(CUtensorMap* m, uint32_t box_rows) const {
   return r == CUDA_SUCCESS;
 }
 
+bool encode_rowmajor_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, bool fp32,
+                        uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr || rows == 0) return false;
+  const uint64_t es = fp32 ? 4 : 2;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * es};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 namespace {
 
 // ------------------------------------------------------------ step bodies ---

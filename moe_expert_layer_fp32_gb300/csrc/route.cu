@@ -689,6 +689,187 @@ __global__ void __launch_bounds__(ClusterCfg<EP, TSV, CC>::NTH)
   }
 }
 
+// ------------------------------------------------ decode (T <= 8): TMA ring ---
+// route_decode_kernel: the sixteen-CTA cluster form for at most eight tokens with
+// the W_r and x copies moved to the tensor memory accelerator.  CTA r owns the
+// EC = EP/16 experts from r*EC; one thread streams boxes of HC hidden rows x EC
+// experts of W_r and HC columns x TSV rows of x into a ring of CNST stages, each
+// completing on its own mbarrier.  The computing threads (one per expert and
+// token) wait on that barrier alone and free a stage with one arrival per warp:
+// no CTA-wide barrier sits inside the FMA chains.  Each logit is the same chain
+// over h = 0..H-1 as in the other kernels, then the bias add; the logits meet in
+// CTA 0, which runs the shared epilogue.  Measured on GB300 against the
+// cp.async form (per-thread 16-byte copies, two CTA barriers per chunk), whose
+// time grew with a deeper ring: see the launcher.
+template <int EP, int TSV>
+struct DecodeCfg {
+  static constexpr int CC = 16;
+  static constexpr int EC = EP / CC;
+  static constexpr int HC = 256;
+  static constexpr int NCMP = EC * TSV;              // computing threads
+  static constexpr int CW = (NCMP + 31) / 32;        // computing warps
+  static constexpr int NTH = 32 * (1 + CW);          // + the copy warp
+  static constexpr int W_BYTES = HC * EC * 4;
+  static constexpr int X_BYTES = TSV * HC * 2;
+  static constexpr int STAGE = W_BYTES + X_BYTES;
+  static constexpr int CNST = (160 * 1024 / STAGE) < 16 ? 160 * 1024 / STAGE : 16;
+  static constexpr int LLD = EP + 1;
+  static constexpr int bytes = 128 + CNST * STAGE + 2 * CNST * 8 + 16 + TSV * LLD * 4;
+  static_assert(EC >= 4 && W_BYTES % 128 == 0 && X_BYTES % 128 == 0, "TMA boxes");
+  static_assert(bytes <= 227 * 1024, "shared memory");
+};
+
+struct DecodeMaps {
+  CUtensorMap w;  // W_r [H][E] FP32, box EC x HC
+  CUtensorMap x;  // x [T][H] BF16, box HC x TSV
+};
+
+// Bounded parity wait without a status word (the router has none): false once
+// *abort is raised or `limit` cycles pass (then it raises *abort).
+__device__ __forceinline__ bool route_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                           long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+template <int EP, int TSV, int KIND>
+__global__ void __launch_bounds__(DecodeCfg<EP, TSV>::NTH)
+    route_decode_kernel(const __grid_constant__ DecodeMaps maps, const float* __restrict__ bias,
+                        int T, int H, int E, int k, int wbf16, int32_t* __restrict__ topk_idx,
+                        float* __restrict__ topk_w, long long spin_limit) {
+  using C = DecodeCfg<EP, TSV>;
+  constexpr int EC = C::EC, HC = C::HC, CNST = C::CNST, LLD = C::LLD;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  uint8_t* sW = base;                                   // [CNST][HC][EC] FP32
+  uint8_t* sX = base + CNST * C::W_BYTES;               // [CNST][TSV][HC] BF16
+  uint64_t* full = reinterpret_cast<uint64_t*>(sX + CNST * C::X_BYTES);
+  uint64_t* empty = full + CNST;
+  int* s_err = reinterpret_cast<int*>(empty + CNST);    // CTA 0's: the cluster's error flag
+  volatile int* abort_flag = s_err + 1;                 // this CTA's
+  float* ls = reinterpret_cast<float*>(s_err + 4);      // [TSV][LLD], CTA 0's used
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = (int)cluster_ctarank();
+  const int e0 = rank * EC;
+  const int t0 = (blockIdx.x / C::CC) * TSV;
+  // a CTA whose experts all lie past E copies and computes nothing
+  const int nchunks = e0 < E ? (H + HC - 1) / HC : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < CNST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::CW);
+    }
+    *s_err = 0;
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&maps.w);
+    prefetch_tensormap(&maps.x);
+  }
+  __syncthreads();
+  // first cluster phase: every CTA's flag is initialised before any remote write
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  // a programmatic dependent launch: x, W_r and the outputs are touched after the
+  // previous kernel finished
+  pdl_wait();
+  if (tid == 0) pdl_launch_dependents();
+
+  float acc = 0.0f;
+  const int ct = tid - 32;
+  const int el = ct % EC, tok = ct / EC;
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- copies
+      int c = 0;
+      for (; c < nchunks; ++c) {
+        const int s = c % CNST;
+        const uint32_t ph = (c / CNST) & 1;
+        if (!route_wait(&empty[s], ph ^ 1, abort_flag, spin_limit)) break;
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        tma_load_2d(&maps.w, sW + s * C::W_BYTES, &full[s], e0, c * HC);
+        tma_load_2d(&maps.x, sX + s * C::X_BYTES, &full[s], c * HC, t0);
+      }
+      if (*abort_flag) {  // let the copies in flight land before the CTA exits
+        for (int i = (c > CNST ? c - CNST : 0); i < c; ++i)
+          wait_drain(&full[i % CNST], (i / CNST) & 1, kSpinLimitCycles);
+      }
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------------- chains
+    const bool active = ct < C::NCMP;
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % CNST;
+      const uint32_t ph = (c / CNST) & 1;
+      const bool ok = __all_sync(0xFFFFFFFFu, route_wait(&full[s], ph, abort_flag, spin_limit));
+      if (!ok) break;
+      if (active) {
+        const int rows = min(HC, H - c * HC);
+        const float* wsb = reinterpret_cast<const float*>(sW + s * C::W_BYTES) + el;
+        const uint16_t* xsb = reinterpret_cast<const uint16_t*>(sX + s * C::X_BYTES) + tok * HC;
+        auto step8 = [&](int hh) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xsb + hh);
+          acc = fmaf(bf16_lo(xv.x), wsb[(hh + 0) * EC], acc);
+          acc = fmaf(bf16_hi(xv.x), wsb[(hh + 1) * EC], acc);
+          acc = fmaf(bf16_lo(xv.y), wsb[(hh + 2) * EC], acc);
+          acc = fmaf(bf16_hi(xv.y), wsb[(hh + 3) * EC], acc);
+          acc = fmaf(bf16_lo(xv.z), wsb[(hh + 4) * EC], acc);
+          acc = fmaf(bf16_hi(xv.z), wsb[(hh + 5) * EC], acc);
+          acc = fmaf(bf16_lo(xv.w), wsb[(hh + 6) * EC], acc);
+          acc = fmaf(bf16_hi(xv.w), wsb[(hh + 7) * EC], acc);
+        };
+        if (rows == HC) {
+#pragma unroll
+          for (int hh = 0; hh < HC; hh += 8) step8(hh);
+        } else {
+#pragma unroll 4
+          for (int hh = 0; hh < rows; hh += 8) step8(hh);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (*abort_flag) {
+    if (tid == 0) {
+      const uint32_t dst = mapa_shared(smem_u32(s_err), 0);
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst), "r"(1) : "memory");
+    }
+  } else if (warp > 0 && ct < C::NCMP && e0 + el < E) {
+    const int e = e0 + el;
+    float l = acc;
+    if (KIND == 0 && bias != nullptr) l = __fadd_rn(l, __ldg(bias + e));
+    const uint32_t dst = mapa_shared(smem_u32(ls + tok * LLD + e), 0);
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(l) : "memory");
+  }
+  cluster_sync();
+  if (rank == 0) {
+    for (int tl = warp; tl < TSV; tl += C::NTH / 32) {
+      const int t = t0 + tl;
+      if (t >= T) continue;
+      if (*s_err) {  // a wait ran out: no routing (the dispatch rejects index -1)
+        if (lane < k) {
+          topk_idx[(size_t)t * k + lane] = -1;
+          topk_w[(size_t)t * k + lane] = 0.0f;
+        }
+      } else {
+        route_one_token<EP, KIND>(ls + tl * LLD, KIND == 1 ? bias : nullptr, E, k, wbf16, lane,
+                                  t, topk_idx, topk_w);
+      }
+    }
+  }
+}
+
 template <int EP, int TSV, int KIND, int CC = kCC>
 cudaError_t launch_cluster(const void* x, const float* wr, const float* bias, int T, int H, int E,
                            int k, int wbf16, int32_t* idx, float* w, cudaStream_t s) {
@@ -736,6 +917,49 @@ cudaError_t launch_cluster(const void* x, const float* wr, const float* bias, in
                             wbf16, idx, w);
 }
 
+template <int EP, int TSV, int KIND>
+cudaError_t launch_decode(const void* x, const float* wr, const float* bias, int T, int H, int E,
+                          int k, int wbf16, int32_t* idx, float* w, cudaStream_t s) {
+  using C = DecodeCfg<EP, TSV>;
+  auto kern = route_decode_kernel<EP, TSV, KIND>;
+  static int ok[64] = {};  // 0: unknown, 1: launchable, -1: a 16-CTA cluster does not fit
+  int dv = 0;
+  cudaGetDevice(&dv);
+  const int known = dv < 64 ? ok[dv] : 0;
+  DecodeMaps m;
+  if (known < 0 || (E % 4) != 0 ||
+      !encode_rowmajor_2d(&m.w, wr, (uint64_t)E, (uint64_t)H, true, C::EC, C::HC) ||
+      !encode_rowmajor_2d(&m.x, x, (uint64_t)H, (uint64_t)T, false, C::HC, TSV))
+    return launch_cluster<EP, TSV, KIND, 16>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C::CC;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  pdl_attr(attr[1]);
+  cfg.gridDim = dim3(C::CC * ((T + TSV - 1) / TSV));
+  cfg.blockDim = dim3(C::NTH);
+  cfg.dynamicSmemBytes = C::bytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (known == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::bytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    int clusters = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess || clusters < 1) {
+      (void)cudaGetLastError();
+      if (dv < 64) ok[dv] = -1;
+      return launch_cluster<EP, TSV, KIND, 16>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    }
+    if (dv < 64) ok[dv] = 1;
+  }
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, m, bias, T, H, E, k, wbf16, idx, w, kSpinLimitCycles);
+}
+
 template <int EP, int KIND>
 cudaError_t launch_ep(const void* x, const float* wr, const float* bias, int T, int H, int E, int k,
                       int wbf16, int32_t* idx, float* w, cudaStream_t s) {
@@ -744,11 +968,16 @@ cudaError_t launch_ep(const void* x, const float* wr, const float* bias, int T, 
     // sixteen CTAs, four or more experts each.  Measured on GB300 (router stage,
     // L2 flushed): large T = 8 38 against 46 us, T = 1 33 against 34 us;
     // fine_grained T = 1 17 against 18 us; at T = 64 eight CTAs were 2 us faster.
-    constexpr int CS = EP >= 64 ? 16 : kCC;
-    if (T == 1) return launch_cluster<EP, 1, KIND, CS>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
-    if (T == 2) return launch_cluster<EP, 2, KIND, CS>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
-    if (T <= 4) return launch_cluster<EP, 4, KIND, CS>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
-    if (T <= 8) return launch_cluster<EP, 8, KIND, CS>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    if constexpr (EP >= 64) {
+      if (T == 1) return launch_decode<EP, 1, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+      if (T == 2) return launch_decode<EP, 2, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+      if (T <= 4) return launch_decode<EP, 4, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+      if (T <= 8) return launch_decode<EP, 8, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    }
+    if (T == 1) return launch_cluster<EP, 1, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    if (T == 2) return launch_cluster<EP, 2, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    if (T <= 4) return launch_cluster<EP, 4, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
+    if (T <= 8) return launch_cluster<EP, 8, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
     return launch_cluster<EP, 8, KIND>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
   }
   // Clusters of eight tokens up to kRouteClusterMaxT.  Measured on GB300 (router

@@ -148,3 +148,27 @@ def test_route_kernels_agree_bitwise(moe):
         np.testing.assert_array_equal(idx, big_idx[:T])
         np.testing.assert_array_equal(w.view(np.uint32), big_w[:T].view(np.uint32))
 
+
+
+@pytest.mark.parametrize("E", [64, 68, 100, 200, 66])
+def test_decode_router_matches_cluster_router(moe, E):
+    """Up to eight tokens run the sixteen-CTA router fed by tensor copies; expert
+    counts that leave the last CTAs partly or wholly past E (68, 100, 200) and one
+    whose W_r rows are not 16-byte multiples (66: the cp.async form) must give the
+    bits of the cluster router that runs from nine tokens, and the oracle's."""
+    wl = synth.Workload("decode_route", T=64, H=1024, E=E, k=8, I=128, w_std=0.05)
+    x = synth.tokens(wl)
+    wr, bias = synth.router(wl)
+    def route(T):
+        d = moe.dims(T, wl.H, wl.E, wl.k, wl.I)
+        idx = torch.empty((T, wl.k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, wl.k), dtype=torch.float32, device="cuda")
+        moe.moe_route(dev_bf16(x[:T]), dev(wr), None if bias is None else dev(bias), d, idx, w)
+        return idx.cpu().numpy(), w.cpu().numpy()
+    ref_idx, ref_w = route(64)
+    for T in (1, 2, 3, 5, 8):
+        idx, w = route(T)
+        np.testing.assert_array_equal(idx, ref_idx[:T])
+        np.testing.assert_array_equal(w.view(np.uint32), ref_w[:T].view(np.uint32))
+    idx_o, w_o = oracle.route(x[:8], wr, bias, wl.k)
+    np.testing.assert_array_equal(route(8)[0], idx_o)
