@@ -208,24 +208,38 @@ __global__ void __launch_bounds__(192, 1)
   }
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = __ldg(offsets + e);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // schedule: validate offsets (0 = o_0 <= o_1 <= ... <= o_E = R), work prefix
-    bool ok = s_off[0] == 0 && s_off[E] == R;
-    int p = 0;
-    for (int e = 0; e < E; ++e) {
-      const int a = s_off[e], b = s_off[e + 1];
-      if (b < a) ok = false;
-      const int tt = b > a ? (b - a + TT - 1) / TT : 0;
-      s_tt[e] = tt;
-      s_prefix[e] = p;
-      p += tt * NTW;
+  if (warp == 0) {
+    // schedule, one warp: validate offsets (0 = o_0 <= o_1 <= ... <= o_E = R),
+    // token tiles per expert and the exclusive prefix of work units, 32 experts
+    // per step (a scan over the lanes)
+    bool ok = true;
+    int carry = 0;
+    for (int eb = 0; eb < E; eb += 32) {
+      const int e = eb + lane;
+      int cnt = 0;
+      if (e < E) {
+        const int a = s_off[e], b = s_off[e + 1];
+        if (b < a) ok = false;
+        const int tt = b > a ? (b - a + TT - 1) / TT : 0;
+        s_tt[e] = tt;
+        cnt = tt * NTW;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += n;
+      }
+      if (e < E) s_prefix[e] = carry + incl - cnt;
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
+    ok = __all_sync(0xFFFFFFFFu, ok) && s_off[0] == 0 && s_off[E] == R;
     if (!ok) {
-      flag_error(status, MOE_ERR_DEVICE_CHECK);
-      for (int e = 0; e < E; ++e) s_prefix[e] = 0;
-      p = 0;
+      for (int e = lane; e < E; e += 32) s_prefix[e] = 0;
+      carry = 0;
+      if (lane == 0) flag_error(status, MOE_ERR_DEVICE_CHECK);
     }
-    s_prefix[E] = p;
+    if (lane == 0) s_prefix[E] = carry;
   }
   tc_fence_before();
   __syncthreads();
