@@ -207,10 +207,17 @@ __device__ __forceinline__ void route_one_token(const float* lrow, const float* 
       if (lane + 32 * q < E) z = __fadd_rn(z, expf(v[q] - m));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) z = __fadd_rn(z, __shfl_xor_sync(0xFFFFFFFFu, z, off));
+    // lane j < k divides its own p_j = exp(l_j - m) / z; every lane then adds
+    // p_0 .. p_{k-1} left to right
+    float lj = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k && j == lane) lj = sel_l[j];
+    const float pl = __fdiv_rn(expf(lj - m), z);
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       if (j < k) {
-        p[j] = __fdiv_rn(expf(sel_l[j] - m), z);
+        p[j] = __shfl_sync(0xFFFFFFFFu, pl, j);
         S = __fadd_rn(S, p[j]);
       }
     }
@@ -223,14 +230,20 @@ __device__ __forceinline__ void route_one_token(const float* lrow, const float* 
       }
     }
   }
+  // lane j < k writes slot j (the k divisions run side by side)
+  float pj = 0.0f;
+  int ej = 0;
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j < k && lane == j) {
-      float wj = __fdiv_rn(p[j], S);
-      if (wbf16) wj = round_bf16(wj);
-      topk_idx[(size_t)t * k + j] = sel_e[j];
-      topk_w[(size_t)t * k + j] = wj;
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < k && j == lane) {
+      pj = p[j];
+      ej = sel_e[j];
     }
+  if (lane < k) {
+    float wj = __fdiv_rn(pj, S);
+    if (wbf16) wj = round_bf16(wj);
+    topk_idx[(size_t)t * k + lane] = ej;
+    topk_w[(size_t)t * k + lane] = wj;
   }
 }
 
@@ -705,23 +718,27 @@ template <int EP, int TSV>
 struct DecodeCfg {
   static constexpr int CC = 16;
   static constexpr int EC = EP / CC;
-  static constexpr int HC = 256;
+  static constexpr int BR = 256;                     // hidden rows per box (the TMA maximum)
+  static constexpr int NB = 2;                       // boxes per stage
+  static constexpr int HC = NB * BR;                 // hidden rows per stage
   static constexpr int NCMP = EC * TSV;              // computing threads
   static constexpr int CW = (NCMP + 31) / 32;        // computing warps
   static constexpr int NTH = 32 * (1 + CW);          // + the copy warp
-  static constexpr int W_BYTES = HC * EC * 4;
-  static constexpr int X_BYTES = TSV * HC * 2;
+  static constexpr int WB_BYTES = BR * EC * 4;       // one W_r box [BR][EC]
+  static constexpr int XB_BYTES = TSV * BR * 2;      // one x box [TSV][BR]
+  static constexpr int W_BYTES = NB * WB_BYTES;
+  static constexpr int X_BYTES = NB * XB_BYTES;
   static constexpr int STAGE = W_BYTES + X_BYTES;
   static constexpr int CNST = (160 * 1024 / STAGE) < 16 ? 160 * 1024 / STAGE : 16;
   static constexpr int LLD = EP + 1;
   static constexpr int bytes = 128 + CNST * STAGE + 2 * CNST * 8 + 16 + TSV * LLD * 4;
-  static_assert(EC >= 4 && W_BYTES % 128 == 0 && X_BYTES % 128 == 0, "TMA boxes");
+  static_assert(EC >= 4 && WB_BYTES % 128 == 0 && XB_BYTES % 128 == 0, "TMA boxes");
   static_assert(bytes <= 227 * 1024, "shared memory");
 };
 
 struct DecodeMaps {
-  CUtensorMap w;  // W_r [H][E] FP32, box EC x HC
-  CUtensorMap x;  // x [T][H] BF16, box HC x TSV
+  CUtensorMap w;  // W_r [H][E] FP32, box EC x BR
+  CUtensorMap x;  // x [T][H] BF16, box BR x TSV
 };
 
 // Bounded parity wait without a status word (the router has none): false once
@@ -794,9 +811,15 @@ __global__ void __launch_bounds__(DecodeCfg<EP, TSV>::NTH)
         const int s = c % CNST;
         const uint32_t ph = (c / CNST) & 1;
         if (!route_wait(&empty[s], ph ^ 1, abort_flag, spin_limit)) break;
-        mbar_arrive_expect_tx(&full[s], C::STAGE);
-        tma_load_2d(&maps.w, sW + s * C::W_BYTES, &full[s], e0, c * HC);
-        tma_load_2d(&maps.x, sX + s * C::X_BYTES, &full[s], c * HC, t0);
+        // boxes that start inside H (none lies wholly past the tensor)
+        const int nbx = min(C::NB, (H - c * HC + C::BR - 1) / C::BR);
+        mbar_arrive_expect_tx(&full[s], nbx * (C::WB_BYTES + C::XB_BYTES));
+        for (int b = 0; b < nbx; ++b) {
+          tma_load_2d(&maps.w, sW + s * C::W_BYTES + b * C::WB_BYTES, &full[s], e0,
+                      c * HC + b * C::BR);
+          tma_load_2d(&maps.x, sX + s * C::X_BYTES + b * C::XB_BYTES, &full[s], c * HC + b * C::BR,
+                      t0);
+        }
       }
       if (*abort_flag) {  // let the copies in flight land before the CTA exits
         for (int i = (c > CNST ? c - CNST : 0); i < c; ++i)
@@ -814,8 +837,11 @@ __global__ void __launch_bounds__(DecodeCfg<EP, TSV>::NTH)
       if (!ok) break;
       if (active) {
         const int rows = min(HC, H - c * HC);
+        // the stage's W_r rows are contiguous over its boxes; its x holds one
+        // [TSV][BR] box after the other
         const float* wsb = reinterpret_cast<const float*>(sW + s * C::W_BYTES) + el;
-        const uint16_t* xsb = reinterpret_cast<const uint16_t*>(sX + s * C::X_BYTES) + tok * HC;
+        const uint16_t* xs0 = reinterpret_cast<const uint16_t*>(sX + s * C::X_BYTES) + tok * C::BR;
+        const uint16_t* xsb = xs0;
         auto step8 = [&](int hh) {
           const uint4 xv = *reinterpret_cast<const uint4*>(xsb + hh);
           acc = fmaf(bf16_lo(xv.x), wsb[(hh + 0) * EC], acc);
@@ -827,12 +853,22 @@ __global__ void __launch_bounds__(DecodeCfg<EP, TSV>::NTH)
           acc = fmaf(bf16_lo(xv.w), wsb[(hh + 6) * EC], acc);
           acc = fmaf(bf16_hi(xv.w), wsb[(hh + 7) * EC], acc);
         };
+        // step8(hh) reads x at xsb + hh: box b's x starts at xs0 + b * (XB - BR) elements
+        // before row b * BR, so xsb moves back by that much for each later box
         if (rows == HC) {
 #pragma unroll
-          for (int hh = 0; hh < HC; hh += 8) step8(hh);
+          for (int b = 0; b < C::NB; ++b) {
+            xsb = xs0 + b * (C::XB_BYTES / 2 - C::BR);
+#pragma unroll
+            for (int hh = b * C::BR; hh < (b + 1) * C::BR; hh += 8) step8(hh);
+          }
         } else {
+          for (int b = 0; b < C::NB && b * C::BR < rows; ++b) {
+            xsb = xs0 + b * (C::XB_BYTES / 2 - C::BR);
+            const int hend = min(rows, (b + 1) * C::BR);
 #pragma unroll 4
-          for (int hh = 0; hh < rows; hh += 8) step8(hh);
+            for (int hh = b * C::BR; hh < hend; hh += 8) step8(hh);
+          }
         }
       }
       __syncwarp();
@@ -928,8 +964,8 @@ cudaError_t launch_decode(const void* x, const float* wr, const float* bias, int
   const int known = dv < 64 ? ok[dv] : 0;
   DecodeMaps m;
   if (known < 0 || (E % 4) != 0 ||
-      !encode_rowmajor_2d(&m.w, wr, (uint64_t)E, (uint64_t)H, true, C::EC, C::HC) ||
-      !encode_rowmajor_2d(&m.x, x, (uint64_t)H, (uint64_t)T, false, C::HC, TSV))
+      !encode_rowmajor_2d(&m.w, wr, (uint64_t)E, (uint64_t)H, true, C::EC, C::BR) ||
+      !encode_rowmajor_2d(&m.x, x, (uint64_t)H, (uint64_t)T, false, C::BR, TSV))
     return launch_cluster<EP, TSV, KIND, 16>(x, wr, bias, T, H, E, k, wbf16, idx, w, s);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];

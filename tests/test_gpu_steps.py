@@ -150,13 +150,15 @@ def test_route_kernels_agree_bitwise(moe):
 
 
 
-@pytest.mark.parametrize("E", [64, 68, 100, 200, 66])
-def test_decode_router_matches_cluster_router(moe, E):
+@pytest.mark.parametrize("E,H", [(64, 1024), (68, 1024), (100, 1024), (200, 1024), (66, 1024),
+                                 (64, 1152), (256, 640)])
+def test_decode_router_matches_cluster_router(moe, E, H):
     """Up to eight tokens run the sixteen-CTA router fed by tensor copies; expert
-    counts that leave the last CTAs partly or wholly past E (68, 100, 200) and one
-    whose W_r rows are not 16-byte multiples (66: the cp.async form) must give the
-    bits of the cluster router that runs from nine tokens, and the oracle's."""
-    wl = synth.Workload("decode_route", T=64, H=1024, E=E, k=8, I=128, w_std=0.05)
+    counts that leave the last CTAs partly or wholly past E (68, 100, 200), one
+    whose W_r rows are not 16-byte multiples (66: the cp.async form) and hidden
+    sizes whose last stage is short (1152, 640) must give the bits of the cluster
+    router that runs from nine tokens, and the oracle's."""
+    wl = synth.Workload("decode_route", T=64, H=H, E=E, k=8, I=128, w_std=0.05)
     x = synth.tokens(wl)
     wr, bias = synth.router(wl)
     def route(T):
