@@ -167,8 +167,9 @@ __global__ void __launch_bounds__(PB) rank_kernel(const int32_t* __restrict__ to
 
 // T <= 256 (a single ranking block): masks, counts, offsets, stable ranks and the
 // row copy in one launch, the work of block_counts + scan + rank + copy_rows.
-// ceil(T / 8) CTAs each rank all T tokens (at most 256 x k ids, from L2) and
-// then copy 8 of them, one warp per token; CTA 0 writes counts and offsets.
+// CTA (b, c) ranks all T tokens (at most 256 x k ids, from L2) and then copies
+// column slice c (of gridDim.y) of tokens 8b..8b+7, one warp per token; the CTAs
+// of slice 0 write the rows, CTA (0, 0) counts and offsets.
 __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __restrict__ topk_idx,
                                                             int T, int k, int E,
                                                             const uint16_t* __restrict__ x, int H,
@@ -185,23 +186,25 @@ __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __res
   __shared__ int s_wsum[PB / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t = blockIdx.x * 8 + warp;  // this warp's token (copy phase)
-  // The token's source row does not depend on the routing: its first 32 x U
-  // 16-byte vectors are loaded now, and land while the CTA ranks.
+  const bool lead = blockIdx.y == 0;
+  // The token's source row does not depend on the routing: the first 32 x U
+  // 16-byte vectors of this CTA's slice are loaded now, and land while it ranks.
   constexpr int U = 8;
-  const int nv = H / 8;  // 16-byte vectors per row
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t < T ? t : 0) * H);
+  const int nvs = H / 8 / gridDim.y;  // 16-byte vectors of the slice
+  const int cb = blockIdx.y * nvs;    // its first vector
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t < T ? t : 0) * H) + cb;
   uint4 v0[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int cc = u * 32 + lane;
-    if (t < T && cc < nv) v0[u] = __ldg(src + cc);
+    if (t < T && cc < nvs) v0[u] = __ldg(src + cc);
   }
   // a programmatic dependent of the router: the routing is read, and every
   // output written, after it has finished (x was final before the router began)
   pdl_wait();
   if (tid == 0) pdl_launch_dependents();
   // every CTA ranks the whole (single) block; each then copies its own 8 tokens
-  build_masks(topk_idx, T, k, E, 0, masks, sidx, blockIdx.x == 0 ? status : nullptr);
+  build_masks(topk_idx, T, k, E, 0, masks, sidx, blockIdx.x == 0 && lead ? status : nullptr);
   int c = 0;
   if (tid < E) {
 #pragma unroll
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __res
     total += sw;
   }
   const int excl = incl - c;
-  if (blockIdx.x == 0) {
+  if (blockIdx.x == 0 && lead) {
     if (tid < E) {
       counts[tid] = c;
       offsets[tid] = excl;
@@ -247,27 +250,29 @@ __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __res
       for (int w = 0; w < tw; ++w) rank += __popc(masks[w * E + e]);
       const long long row = (long long)s_scan[e] + rank;
       if (row >= 0 && row < R) my_row = (int)row;
-      else flag_error(status, MOE_ERR_DEVICE_CHECK);
+      else if (lead) flag_error(status, MOE_ERR_DEVICE_CHECK);
     }
-    row_of_slot[sl] = my_row;
-    if (my_row >= 0) slot_of_row[my_row] = (int32_t)sl;
+    if (lead) {
+      row_of_slot[sl] = my_row;
+      if (my_row >= 0) slot_of_row[my_row] = (int32_t)sl;
+    }
   }
-  for (int c0 = 0; c0 < nv; c0 += 32 * U) {
+  for (int c0 = 0; c0 < nvs; c0 += 32 * U) {
     uint4 v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int cc = c0 + u * 32 + lane;
       if (c0 == 0) v[u] = v0[u];
-      else if (cc < nv) v[u] = __ldg(src + cc);
+      else if (cc < nvs) v[u] = __ldg(src + cc);
     }
     for (int j = 0; j < k; ++j) {
       const int r = __shfl_sync(0xFFFFFFFFu, my_row, j);
       if (r < 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * H);
+      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * H) + cb;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int cc = c0 + u * 32 + lane;
-        if (cc < nv) dst[cc] = v[u];
+        if (cc < nvs) dst[cc] = v[u];
       }
     }
   }
@@ -386,9 +391,16 @@ cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, 
                                   int32_t* slot_of_row, void* x_perm, int32_t* status,
                                   cudaStream_t s) {
   const int nb = T > 0 ? (T + 7) / 8 : 1;
-  return launch_pdl(dispatch_small_kernel, dim3(nb), dim3(PB), mask_smem_bytes(E, k), s, topk_idx,
-                    T, k, E, static_cast<const uint16_t*>(x), H, counts, offsets, row_of_slot,
-                    slot_of_row, static_cast<uint16_t*>(x_perm), status);
+  // column slices of at least 32 vectors (one per lane) while the grid stays
+  // within two CTAs per SM
+  int split = 1;
+  const int nv = H / 8;
+  while (split < 16 && nv % (2 * split) == 0 && nv / (2 * split) >= 32 &&
+         (long long)nb * 2 * split <= 2LL * device_sm_count())
+    split *= 2;
+  return launch_pdl(dispatch_small_kernel, dim3(nb, split), dim3(PB), mask_smem_bytes(E, k), s,
+                    topk_idx, T, k, E, static_cast<const uint16_t*>(x), H, counts, offsets,
+                    row_of_slot, slot_of_row, static_cast<uint16_t*>(x_perm), status);
 }
 
 namespace {
