@@ -24,7 +24,10 @@ namespace {
 
 // SPLIT: gridDim.y CTAs share a token's columns.  That form is held to the
 // unsplit kernel's register count (five CTAs per SM) by its launch bound.
-template <bool SPLIT>
+// A programmatic dependent of the down GEMM: y is read (and out written) only after
+// that kernel has finished.  EARLY: the weights and rows were final before the
+// down GEMM started (the layer's own chain), so they are read before the wait.
+template <bool SPLIT, bool EARLY>
 __global__ void __launch_bounds__(128, SPLIT ? 5 : 0) combine_kernel(const float* __restrict__ y,
                                                       const float* __restrict__ topk_w,
                                                       const int32_t* __restrict__ row_of_slot,
@@ -34,15 +37,17 @@ __global__ void __launch_bounds__(128, SPLIT ? 5 : 0) combine_kernel(const float
   __shared__ float s_w[kMaxK];
   const int t = blockIdx.x;
   const long long R = (long long)T * k;
-  // a programmatic dependent of the down GEMM: y, the weights and the rows are
-  // read (and out written) only after it has finished
+  auto load_slots = [&]() {
+    if (threadIdx.x < k) {
+      const int r = row_of_slot[(size_t)t * k + threadIdx.x];
+      s_row[threadIdx.x] = (r >= 0 && r < R) ? r : -1;
+      s_w[threadIdx.x] = __fmul_rn(scale, topk_w[(size_t)t * k + threadIdx.x]);
+    }
+  };
+  if (EARLY) load_slots();
   pdl_wait();
   if (threadIdx.x == 0) pdl_launch_dependents();
-  if (threadIdx.x < k) {
-    const int r = row_of_slot[(size_t)t * k + threadIdx.x];
-    s_row[threadIdx.x] = (r >= 0 && r < R) ? r : -1;
-    s_w[threadIdx.x] = __fmul_rn(scale, topk_w[(size_t)t * k + threadIdx.x]);
-  }
+  if (!EARLY) load_slots();
   __syncthreads();
   int row[kMaxK];
   float w[kMaxK];
@@ -82,7 +87,8 @@ __global__ void __launch_bounds__(128, SPLIT ? 5 : 0) combine_kernel(const float
 }  // namespace
 
 cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, int T,
-                           int H, int k, float scale, void* out, cudaStream_t s) {
+                           int H, int k, float scale, void* out, cudaStream_t s,
+                           bool slots_final) {
   if (T == 0) return cudaSuccess;
   // split the columns of each token over up to H / 512 CTAs while the grid stays
   // within four CTAs per SM (one wave)
@@ -90,11 +96,15 @@ cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* r
   while (split * 2 <= H / 512 && H % (split * 2 * 512) == 0 &&
          (long long)T * split * 2 <= 4LL * device_sm_count())
     split *= 2;
+  auto go = [&](auto kern, dim3 grid) {
+    return launch_pdl(kern, grid, dim3(128), 0, s, y, topk_w, row_of_slot, T, H, k, scale,
+                      static_cast<uint16_t*>(out));
+  };
   if (split > 1)
-    return launch_pdl(combine_kernel<true>, dim3(T, split), dim3(128), 0, s, y, topk_w,
-                      row_of_slot, T, H, k, scale, static_cast<uint16_t*>(out));
-  return launch_pdl(combine_kernel<false>, dim3(T), dim3(128), 0, s, y, topk_w, row_of_slot, T, H,
-                    k, scale, static_cast<uint16_t*>(out));
+    return slots_final ? go(combine_kernel<true, true>, dim3(T, split))
+                       : go(combine_kernel<true, false>, dim3(T, split));
+  return slots_final ? go(combine_kernel<false, true>, dim3(T))
+                     : go(combine_kernel<false, false>, dim3(T));
 }
 
 }  // namespace moe

@@ -66,14 +66,16 @@ constexpr int kTT = 64;                      // token rows per unit at most (MMA
 // rows (T <= 2 for k = 8).  The down GEMM is a programmatic dependent launch of
 // the gate/up GEMM: its CTAs start on SMs with room while the gate/up GEMM runs
 // and stream their first weight stages before they wait for h.  The TT = 16
-// quarter and half units hold five stages of 16 KB + a 2 KB token box (at most
-// ~110 KB), so a gate/up CTA and a down CTA fit on one SM together.
+// quarter and half units hold five and six stages of 16 KB + a 2 KB token box
+// (about 100 and 115 KB), so a gate/up CTA and a down CTA fit on one SM together.
 template <int HV, int TT = kTT>
 struct SwapCfg {
   static constexpr int UROWS = HV == 2 ? 2 * HALF : HALF;  // weight rows per unit
   static constexpr int NMMA = HV == 2 ? 2 : 1;             // M = 128 MMAs per K step
   static constexpr int X_BYTES = TT * SK * 2;              // token box (N = TT)
-  static constexpr int STAGES = (HV == 2 || TT == 16) ? 5 : 8;
+  // TT = 16: five stages for gate/up units, six for half (down) units, so the
+  // down CTA holds more of its weights before its wait (the pair still fits)
+  static constexpr int STAGES = HV == 2 ? 5 : (TT == 16 ? (HV == 1 ? 6 : 5) : 8);
   static constexpr int W_BYTES = UROWS * SK * 2;           // 32 or 16 KB
   static constexpr int HOFF = TT < 32 ? 32 : TT;           // TMEM columns per half (32-aligned)
   static constexpr int ACC_COLS = NMMA * HOFF;             // one accumulator buffer
@@ -83,8 +85,12 @@ struct SwapCfg {
   static constexpr int XCH_BYTES = HV == 4 ? 64 * (TT + 1) * 4 : 0;
   static constexpr int SMEM_BYTES = 1024 + STAGES * (W_BYTES + X_BYTES) + XCH_BYTES + NBAR * 8 +
                                     16 + 3 * (kMaxE + 1) * 4;
-  static_assert(SMEM_BYTES <= (TT == 16 && HV != 2 ? 110 : 227) * 1024, "shared memory");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
+// a gate/up quarter-unit CTA and a down half-unit CTA on one SM (228 KB, 1 KB each
+// reserved)
+static_assert(SwapCfg<4, 16>::SMEM_BYTES + SwapCfg<1, 16>::SMEM_BYTES + 2048 <= 228 * 1024,
+              "co-resident TT = 16 units");
 
 // Weight boxes (UROWS rows; 64 for HV = 4) and token boxes of 16, 32 and 64 rows;
 // all 64 columns.

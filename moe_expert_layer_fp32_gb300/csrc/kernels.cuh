@@ -124,8 +124,11 @@ cudaError_t launch_gemm_down_swap(const GemmOperand& a, const GemmOperand& b,
                                   int32_t* status, long long spin_limit, cudaStream_t s);
 
 // out[t] = bf16(slot-order FMA chain of (scale * topk_w[t,j]) * y[row_of_slot[t*k+j]])
+// slots_final: topk_w and row_of_slot were complete before the kernel that writes
+// y began (so they may be read before the kernel waits for y)
 cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* row_of_slot, int T,
-                           int H, int k, float scale, void* out, cudaStream_t s);
+                           int H, int k, float scale, void* out, cudaStream_t s,
+                           bool slots_final = false);
 
 // Sharded combine: G per-rank BF16 partials (slot-order FP32 chains, other ranks'
 // slots as exact zeros, optional shared [G][T][H] FP32 added before the rounding)

@@ -380,7 +380,9 @@ moe_status layer_fwd(const void* x, const float* w_router, const float* bias,
     return MOE_OK;
   }
   MOE_TRY(mark(5));
-  if (d.T > 0) MOE_CUDA(launch_combine(y, w, ros, d.T, d.H, d.k, opts.route_scale, out, s));
+  // the routing and the rows were written before the expert GEMMs began
+  if (d.T > 0)
+    MOE_CUDA(launch_combine(y, w, ros, d.T, d.H, d.k, opts.route_scale, out, s, true));
   MOE_TRY(mark(6));
   return MOE_OK;
 }
