@@ -22,13 +22,13 @@
 namespace moe {
 namespace {
 
-// SPLIT: gridDim.y CTAs share a token's columns.  That form is held to the
-// unsplit kernel's register count (five CTAs per SM) by its launch bound.
+// SPLIT: gridDim.y CTAs share a token's columns.  Both forms are held to five CTAs
+// per SM (at most 96 registers) by the launch bound.
 // A programmatic dependent of the down GEMM: y is read (and out written) only after
 // that kernel has finished.  EARLY: the weights and rows were final before the
 // down GEMM started (the layer's own chain), so they are read before the wait.
 template <bool SPLIT, bool EARLY>
-__global__ void __launch_bounds__(128, SPLIT ? 5 : 0) combine_kernel(const float* __restrict__ y,
+__global__ void __launch_bounds__(128, 5) combine_kernel(const float* __restrict__ y,
                                                       const float* __restrict__ topk_w,
                                                       const int32_t* __restrict__ row_of_slot,
                                                       int T, int H, int k, float scale,
