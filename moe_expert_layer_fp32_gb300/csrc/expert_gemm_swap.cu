@@ -44,6 +44,11 @@
 // producer, warp 1 lane 0 MMA issuer, warps 2..5 epilogue (TMEM lane quarter =
 // warp % 4); every wait has a clock limit and an abort path that drains this
 // CTA's own copies and MMAs before tensor memory is freed.
+//
+// Both GEMMs are programmatic dependent launches (pdl.cuh).  The gate/up GEMM
+// waits for its predecessor (the dispatch) before reading the offsets; the down
+// GEMM reads the offsets at once, builds its schedule and issues its first weight
+// stages, and waits for the gate/up GEMM only before its first token (h) copy.
 #include <algorithm>
 
 #include "common.cuh"
