@@ -170,6 +170,9 @@ __global__ void __launch_bounds__(PB) rank_kernel(const int32_t* __restrict__ to
 // CTA (b, c) ranks all T tokens (at most 256 x k ids, from L2) and then copies
 // column slice c (of gridDim.y) of tokens 8b..8b+7, one warp per token; the CTAs
 // of slice 0 write the rows, CTA (0, 0) counts and offsets.
+// LATE: no row copy; the indices are computed first and the kernel waits for its
+// predecessor only at the end (so its completion implies the predecessor's).
+template <bool LATE>
 __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __restrict__ topk_idx,
                                                             int T, int k, int E,
                                                             const uint16_t* __restrict__ x, int H,
@@ -197,12 +200,14 @@ __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __res
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const int cc = u * 32 + lane;
-    if (t < T && cc < nvs) v0[u] = __ldg(src + cc);
+    if (!LATE && t < T && cc < nvs) v0[u] = __ldg(src + cc);
   }
   // a programmatic dependent of the router: the routing is read, and every
   // output written, after it has finished (x was final before the router began)
-  pdl_wait();
-  if (tid == 0) pdl_launch_dependents();
+  if constexpr (!LATE) {
+    pdl_wait();
+    if (tid == 0) pdl_launch_dependents();
+  }
   // every CTA ranks the whole (single) block; each then copies its own 8 tokens
   build_masks(topk_idx, T, k, E, 0, masks, sidx, blockIdx.x == 0 && lead ? status : nullptr);
   int c = 0;
@@ -257,22 +262,27 @@ __global__ void __launch_bounds__(PB) dispatch_small_kernel(const int32_t* __res
       if (my_row >= 0) slot_of_row[my_row] = (int32_t)sl;
     }
   }
-  for (int c0 = 0; c0 < nvs; c0 += 32 * U) {
-    uint4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int cc = c0 + u * 32 + lane;
-      if (c0 == 0) v[u] = v0[u];
-      else if (cc < nvs) v[u] = __ldg(src + cc);
-    }
-    for (int j = 0; j < k; ++j) {
-      const int r = __shfl_sync(0xFFFFFFFFu, my_row, j);
-      if (r < 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * H) + cb;
+  if constexpr (LATE) {
+    pdl_wait();
+    if (tid == 0) pdl_launch_dependents();
+  } else {
+    for (int c0 = 0; c0 < nvs; c0 += 32 * U) {
+      uint4 v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int cc = c0 + u * 32 + lane;
-        if (cc < nvs) dst[cc] = v[u];
+        if (c0 == 0) v[u] = v0[u];
+        else if (cc < nvs) v[u] = __ldg(src + cc);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xFFFFFFFFu, my_row, j);
+        if (r < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * H) + cb;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int cc = c0 + u * 32 + lane;
+          if (cc < nvs) dst[cc] = v[u];
+        }
       }
     }
   }
@@ -391,6 +401,10 @@ cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, 
                                   int32_t* slot_of_row, void* x_perm, int32_t* status,
                                   cudaStream_t s) {
   const int nb = T > 0 ? (T + 7) / 8 : 1;
+  if (x_perm == nullptr)
+    return launch_pdl(dispatch_small_kernel<true>, dim3(nb, 1), dim3(PB), mask_smem_bytes(E, k),
+                      s, topk_idx, T, k, E, static_cast<const uint16_t*>(x), H, counts, offsets,
+                      row_of_slot, slot_of_row, static_cast<uint16_t*>(x_perm), status);
   // column slices of at least 32 vectors (one per lane) while the grid stays
   // within two CTAs per SM
   int split = 1;
@@ -398,9 +412,10 @@ cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, 
   while (split < 16 && nv % (2 * split) == 0 && nv / (2 * split) >= 32 &&
          (long long)nb * 2 * split <= 2LL * device_sm_count())
     split *= 2;
-  return launch_pdl(dispatch_small_kernel, dim3(nb, split), dim3(PB), mask_smem_bytes(E, k), s,
-                    topk_idx, T, k, E, static_cast<const uint16_t*>(x), H, counts, offsets,
-                    row_of_slot, slot_of_row, static_cast<uint16_t*>(x_perm), status);
+  return launch_pdl(dispatch_small_kernel<false>, dim3(nb, split), dim3(PB),
+                    mask_smem_bytes(E, k), s, topk_idx, T, k, E, static_cast<const uint16_t*>(x),
+                    H, counts, offsets, row_of_slot, slot_of_row, static_cast<uint16_t*>(x_perm),
+                    status);
 }
 
 namespace {

@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(192, 1)
     grouped_gemm_swap_kernel(const __grid_constant__ SwapMaps maps,
                              const int32_t* __restrict__ offsets, int E, int R, int n_per_expert,
                              int K, void* __restrict__ out, int out_ld, int32_t* status,
-                             long long spin_limit, int a_local) {
+                             long long spin_limit, int a_local, const int32_t* one_token_ids,
+                             int k_ids) {
   using C = SwapCfg<HV, TT>;
   static_assert(SWIGLU ? HV != 1 : HV != 4, "gate and up rows of a unit must meet in one CTA");
   constexpr int STAGES = C::STAGES, W_BYTES = C::W_BYTES, ACC_COLS = C::ACC_COLS;
@@ -217,7 +218,28 @@ __global__ void __launch_bounds__(192, 1)
     pdl_wait();
     if (threadIdx.x == 0) pdl_launch_dependents();
   }
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = __ldg(offsets + e);
+  if (one_token_ids == nullptr) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = __ldg(offsets + e);
+  } else if (warp == 0) {
+    // one token (R = k_ids rows): the offsets of the stable permutation follow from
+    // its k distinct expert ids, o_e = #{j : id_j < e}; a bad or repeated id
+    // leaves o_E = 0 != R, which the check below rejects
+    const int id = lane < k_ids ? __ldg(one_token_ids + lane) : -1;
+    bool bad = lane < k_ids && (id < 0 || id >= E);
+    int ids[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      ids[j] = __shfl_sync(0xFFFFFFFFu, id, j);
+      if (j < k_ids && j != lane && lane < k_ids && ids[j] == id) bad = true;
+    }
+    bad = __any_sync(0xFFFFFFFFu, bad);
+    for (int e = lane; e <= E; e += 32) {
+      int c = 0;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) c += (j < k_ids && ids[j] < e) ? 1 : 0;
+      s_off[e] = bad ? 0 : c;
+    }
+  }
   __syncthreads();
   if (warp == 0) {
     // schedule, one warp: validate offsets (0 = o_0 <= o_1 <= ... <= o_E = R),
@@ -446,7 +468,8 @@ __global__ void __launch_bounds__(192, 1)
 template <bool SWIGLU, int HV, int TT>
 cudaError_t launch_swap_tt(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets,
                            int E, int R, int n_per_expert, int K, void* out, int out_ld,
-                           int32_t* status, long long spin_limit, cudaStream_t s, int a_local) {
+                           int32_t* status, long long spin_limit, cudaStream_t s, int a_local,
+                           const int32_t* one_token_ids) {
   SwapMaps m;
   using C = SwapCfg<HV, TT>;
   // both GEMMs are programmatic dependent launches; the down GEMM (DEP) streams
@@ -479,8 +502,9 @@ cudaError_t launch_swap_tt(const GemmOperand& a, const GemmOperand& b, const int
   pdl_attr(attr[0]);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // one token: k_ids = R
   return cudaLaunchKernelEx(&cfg, kern, m, offsets, E, R, n_per_expert, K, out, out_ld, status,
-                            spin_limit, a_local);
+                            spin_limit, a_local, one_token_ids, R);
 }
 
 // TT = 16 when the whole batch has at most 16 rows (every expert then has at most
@@ -488,12 +512,13 @@ cudaError_t launch_swap_tt(const GemmOperand& a, const GemmOperand& b, const int
 template <bool SWIGLU, int HV>
 cudaError_t launch_swap(const GemmOperand& a, const GemmOperand& b, const int32_t* offsets, int E,
                         int R, int n_per_expert, int K, void* out, int out_ld, int32_t* status,
-                        long long spin_limit, cudaStream_t s, int a_local) {
+                        long long spin_limit, cudaStream_t s, int a_local,
+                        const int32_t* one_token_ids = nullptr) {
   if (R <= 16)
     return launch_swap_tt<SWIGLU, HV, 16>(a, b, offsets, E, R, n_per_expert, K, out, out_ld,
-                                          status, spin_limit, s, a_local);
+                                          status, spin_limit, s, a_local, one_token_ids);
   return launch_swap_tt<SWIGLU, HV, kTT>(a, b, offsets, E, R, n_per_expert, K, out, out_ld, status,
-                                         spin_limit, s, a_local);
+                                         spin_limit, s, a_local, one_token_ids);
 }
 
 }  // namespace
@@ -513,27 +538,32 @@ bool use_swap_gemm(int E, int R, int H, int I) {
 cudaError_t launch_gemm_gate_up_swap(const GemmOperand& a, const GemmOperand& b,
                                      const int32_t* offsets, int E, int R, int H, int I, void* h,
                                      int32_t* status, long long spin_limit, cudaStream_t s,
-                                     bool a_local) {
+                                     bool a_local, const int32_t* one_token_ids) {
   if (R == 0) return cudaSuccess;
+  // one token: every expert's single row is the token itself (A rows from 0)
+  const int al = (a_local || one_token_ids != nullptr) ? 1 : 0;
   // quarter units (64 gate + 64 up rows) while whole-box units would fill at most
   // half of the SMs (experts with rows <= min(E, R)); each element's chain and
   // epilogue arithmetic are the same
   if (2LL * (2 * I / WROWS) * std::min(E, R) <= device_sm_count())
-    return launch_swap<true, 4>(a, b, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
-                                a_local ? 1 : 0);
-  return launch_swap<true, 2>(a, b, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s,
-                           a_local ? 1 : 0);
+    return launch_swap<true, 4>(a, b, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s, al,
+                                one_token_ids);
+  return launch_swap<true, 2>(a, b, offsets, E, R, 2 * I, H, h, I, status, spin_limit, s, al,
+                              one_token_ids);
 }
 
 cudaError_t launch_gemm_down_swap(const GemmOperand& a, const GemmOperand& b,
                                   const int32_t* offsets, int E, int R, int H, int I, float* y,
-                                  int32_t* status, long long spin_limit, cudaStream_t s) {
+                                  int32_t* status, long long spin_limit, cudaStream_t s,
+                                  const int32_t* one_token_ids) {
   if (R == 0) return cudaSuccess;
   // half-box units while whole-box units would fill at most half of the SMs
   // (experts with rows <= min(E, R)); each row's chain and epilogue are the same
   if (2LL * (H / WROWS) * std::min(E, R) <= device_sm_count())
-    return launch_swap<false, 1>(a, b, offsets, E, R, H, I, y, H, status, spin_limit, s, 0);
-  return launch_swap<false, 2>(a, b, offsets, E, R, H, I, y, H, status, spin_limit, s, 0);
+    return launch_swap<false, 1>(a, b, offsets, E, R, H, I, y, H, status, spin_limit, s, 0,
+                                 one_token_ids);
+  return launch_swap<false, 2>(a, b, offsets, E, R, H, I, y, H, status, spin_limit, s, 0,
+                               one_token_ids);
 }
 
 }  // namespace moe

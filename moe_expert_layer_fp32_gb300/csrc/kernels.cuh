@@ -57,6 +57,9 @@ cudaError_t launch_uniform_offsets(int32_t* offsets, int G, int T, cudaStream_t 
 
 // T <= kPermBlock: counts, offsets, row_of_slot, slot_of_row and the permuted
 // rows x_perm in one launch
+// x_perm == nullptr (late): the indices only, computed before the kernel waits for
+// its predecessor (which must neither read nor write them); the kernel then waits, so
+// its completion implies the predecessor's
 cudaError_t launch_dispatch_small(const int32_t* topk_idx, int T, int k, int E, const void* x,
                                   int H, int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
                                   int32_t* slot_of_row, void* x_perm, int32_t* status,
@@ -115,13 +118,18 @@ int gemm_down_bn(int H);
 // most four gate/up work units per SM (experts with rows <= min(E, R)).
 constexpr int kSwapRowsPerExpert = 8;
 bool use_swap_gemm(int E, int R, int H, int I);
+// one_token_ids (a batch of one token, R = k): the schedule comes from the token's
+// k expert ids instead of `offsets` (the same rows: expert e's row is the number of
+// chosen experts below e), so the GEMMs need not wait for the dispatch; the gate/up
+// GEMM then reads the token row itself (a = x [1, H]).
 cudaError_t launch_gemm_gate_up_swap(const GemmOperand& a, const GemmOperand& b,
                                      const int32_t* offsets, int E, int R, int H, int I, void* h,
                                      int32_t* status, long long spin_limit, cudaStream_t s,
-                                     bool a_local = false);
+                                     bool a_local = false, const int32_t* one_token_ids = nullptr);
 cudaError_t launch_gemm_down_swap(const GemmOperand& a, const GemmOperand& b,
                                   const int32_t* offsets, int E, int R, int H, int I, float* y,
-                                  int32_t* status, long long spin_limit, cudaStream_t s);
+                                  int32_t* status, long long spin_limit, cudaStream_t s,
+                                  const int32_t* one_token_ids = nullptr);
 
 // out[t] = bf16(slot-order FMA chain of (scale * topk_w[t,j]) * y[row_of_slot[t*k+j]])
 // slots_final: topk_w and row_of_slot were complete before the kernel that writes

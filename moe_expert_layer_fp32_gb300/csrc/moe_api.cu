@@ -221,9 +221,13 @@ moe_status do_permute_rows(const void* x, const int32_t* idx, const moe_dims& d,
   return MOE_OK;
 }
 
+// token_ids (one token, the swapped form): the GEMMs take their rows from the
+// token's k expert ids and the gate/up GEMM reads the token row x_token itself, so
+// neither x_perm nor offsets is read
 moe_status do_expert_ffn(const void* x_perm, const int32_t* offsets, const void* packed,
                          const moe_dims& d, float* y, void* ws, cudaStream_t s,
-                         cudaEvent_t after_gate_up = nullptr) {
+                         cudaEvent_t after_gate_up = nullptr, const void* x_token = nullptr,
+                         const int32_t* token_ids = nullptr) {
   const Layout L = layout(d);
   const int R = d.T * d.k;
   if (R == 0) return MOE_OK;
@@ -231,7 +235,8 @@ moe_status do_expert_ffn(const void* x_perm, const int32_t* offsets, const void*
   void* h = at<void>(ws, L.h);
   const uint16_t* w1 = static_cast<const uint16_t*>(packed);
   const uint16_t* w2 = w1 + (size_t)d.E * 2 * d.I * d.H;
-  const GemmOperand ma{x_perm, (uint64_t)d.H, (uint64_t)R};
+  const GemmOperand ma{token_ids != nullptr ? x_token : x_perm, (uint64_t)d.H,
+                       (uint64_t)(token_ids != nullptr ? d.T : R)};
   // packed weights are box-tiled: 64 K values per row, (expert, column tile, k-block) boxes
   const GemmOperand mb{w1, 64, (uint64_t)d.E * 2 * d.I * (d.H / 64)};
   const GemmOperand mh{h, (uint64_t)d.I, (uint64_t)R};
@@ -239,13 +244,16 @@ moe_status do_expert_ffn(const void* x_perm, const int32_t* offsets, const void*
   // few rows per expert: weight rows on the MMA's M side (same bits as the tiles)
   const bool swap = use_swap_gemm(d.E, R, d.H, d.I);
   const long long lim = g_wait_limit.load();
+  if (token_ids != nullptr && !(swap && d.T == 1)) return MOE_ERR_INVALID_ARG;
   if (swap)
-    MOE_CUDA(launch_gemm_gate_up_swap(ma, mb, offsets, d.E, R, d.H, d.I, h, status, lim, s));
+    MOE_CUDA(launch_gemm_gate_up_swap(ma, mb, offsets, d.E, R, d.H, d.I, h, status, lim, s, false,
+                                      token_ids));
   else
     MOE_CUDA(launch_gemm_gate_up(ma, mb, offsets, d.E, R, d.H, d.I, h, status, lim, s));
   if (after_gate_up != nullptr) MOE_CUDA(cudaEventRecord(after_gate_up, s));
   if (swap)
-    MOE_CUDA(launch_gemm_down_swap(mh, md, offsets, d.E, R, d.H, d.I, y, status, lim, s));
+    MOE_CUDA(launch_gemm_down_swap(mh, md, offsets, d.E, R, d.H, d.I, y, status, lim, s,
+                                   token_ids));
   else
     MOE_CUDA(launch_gemm_down(mh, md, offsets, d.E, R, d.H, d.I, y, status, lim, s));
   return MOE_OK;
@@ -347,6 +355,16 @@ moe_status layer_fwd(const void* x, const float* w_router, const float* bias,
   MOE_CUDA(launch_route(x, w_router, bias, d.T, d.H, d.E, d.k, opts.kind, opts.weights_bf16, idx,
                         w, s));
   MOE_TRY(mark(1));
+  if (d.T == 1 && ev == nullptr && shard == nullptr && use_swap_gemm(d.E, d.k, d.H, d.I)) {
+    // One token: both GEMMs take their rows from the token's expert ids and the
+    // gate/up GEMM reads the token row itself, so the dispatch (indices only) runs
+    // after them and off their path; the combine then reads the rows after its wait.
+    MOE_TRY(do_expert_ffn(nullptr, offsets, packed_weights, d, y, workspace, s, nullptr, x, idx));
+    MOE_CUDA(launch_dispatch_small(idx, d.T, d.k, d.E, x, d.H, counts, offsets, ros, sor, nullptr,
+                                   at<int32_t>(workspace, L.status), s));
+    MOE_CUDA(launch_combine(y, w, ros, d.T, d.H, d.k, opts.route_scale, out, s, false));
+    return MOE_OK;
+  }
   if (d.T > 0 && d.T <= kPermBlock) {
     // one ranking block: counts, offsets, ranks and the row copy in a single
     // launch (the load-statistics stage holds the permute; mark 2 closes both)
