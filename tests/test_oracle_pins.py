@@ -252,6 +252,27 @@ def test_permutation_is_stable_bijection(T, E, k):
         assert ros[s] == offsets[e] + int((idx[:t] == e).any(axis=1).sum())
 
 
+@pytest.mark.parametrize("E,k", [(8, 2), (64, 8), (128, 8), (256, 16)])
+def test_one_token_rows_follow_from_its_expert_ids(E, k):
+    """For a batch of one token the stable permutation is fixed by the token's k
+    distinct expert ids alone: offsets[e] = #{j : id_j < e} and the row of slot j
+    is offsets[id_j].  The one-token decode path schedules both expert GEMMs by
+    this formula before the dispatch has run; here it is checked against the
+    oracle's load statistics and permutation."""
+    H = 16
+    for seed in range(5):
+        x = synth.normal_bf16(11 + seed, synth.TID_X, (1, H), 1.0)
+        wr = synth.normal_f32(11 + seed, synth.TID_WR, (H, E), 1.0)
+        idx, _ = oracle.route(x, wr, None, k)
+        ids = idx[0]
+        assert len(set(ids.tolist())) == k
+        counts, offsets, _, _ = oracle.load_stats(idx, E)
+        _, ros, _ = oracle.permute(x, idx, offsets, E, with_x_perm=False)
+        formula = np.array([int((ids < e).sum()) for e in range(E + 1)], dtype=np.int32)
+        np.testing.assert_array_equal(offsets, formula)
+        np.testing.assert_array_equal(ros, formula[ids])
+
+
 # ------------------------------------------------------------- expert FFN ---
 def test_swiglu_one_round_golden():
     """silu(g)*u in FP32, one BF16 round, identity down projection.  Catches gate
