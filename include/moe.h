@@ -332,7 +332,12 @@ moe_status moe_layer_fwd_sharded_profiled(
  *   x [T, H] bf16; w_router [H, E] fp32; bias [E] fp32 or NULL; packed_weights
  *   from moe_prepack_expert_weights; out [T, H] bf16.
  *   topk_idx_out [T, k], topk_w_out [T, k] and counts_out [E] are optional
- *   (NULL: kept in the workspace only). */
+ *   (NULL: kept in the workspace only).
+ * Stream order is that of ordinary launches for every other kernel: the layer's
+ * own kernels may start while the previous one of them runs (programmatic
+ * dependent launch) but touch its outputs only after it has finished.  For a
+ * one-token batch the small-batch expert GEMMs run before the load statistics
+ * (their rows follow from the token's expert ids); every output is the same. */
 moe_status moe_layer_fwd(const void* x, const float* w_router, const float* bias,
                          const void* packed_weights, moe_dims d, void* out, int32_t* topk_idx_out,
                          float* topk_w_out, int32_t* counts_out, void* workspace, size_t ws_bytes,
